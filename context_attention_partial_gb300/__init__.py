@@ -1,2 +1,14 @@
-"""GB300-native context-parallel attention kernels (placeholder: the library
-binding lands with the C-ABI)."""
+"""GB300-native hot path of context-parallel attention (Ring, Ring Anything,
+Ulysses) on one GPU: hand-written sm_103a CUDA kernels behind the C ABI in
+include/cpattn.h, with this thin PyTorch binding on top.
+
+The shared library is loaded on first use and must exist (built by
+``__graft_entry__.build()``); there is no CPU fallback.
+"""
+from .api import (CpattnError, grouped_as_bhsd, last_device_status, merge, partial, ring,
+                  ring_workspace_bytes, set_wait_timeout_ns, ulysses_attention, ulysses_permute)
+from ._lib import EXPORTS, LIB_PATH, load as load_library
+
+__all__ = ["partial", "merge", "ring", "ring_workspace_bytes", "ulysses_permute",
+           "ulysses_attention", "grouped_as_bhsd", "last_device_status", "set_wait_timeout_ns",
+           "CpattnError", "EXPORTS", "LIB_PATH", "load_library"]

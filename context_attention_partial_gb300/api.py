@@ -1,0 +1,163 @@
+"""PyTorch-facing binding of libcpattn.so.
+
+Argument marshalling only: every function here allocates outputs with
+PyTorch when the caller did not pass them, describes the tensors to the C ABI
+and calls it on the current CUDA stream.  All computation runs in the CUDA
+kernels; CPU tensors are rejected (there is no CPU path).
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import CpattnError, check, describe
+
+_DTYPES = {torch.float32: _lib.F32, torch.bfloat16: _lib.BF16}
+
+
+def _code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"dtype {t.dtype} is not supported (float32 or bfloat16)") from None
+
+
+def _desc(t: torch.Tensor) -> _lib.CTensor:
+    if not t.is_cuda:
+        raise ValueError("cpattn runs on CUDA tensors only (no CPU path)")
+    return describe(t.data_ptr(), _code(t), t.shape, t.stride())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _scale(scale: Optional[float]) -> float:
+    return 0.0 if scale is None else float(scale)
+
+
+def partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """One ring step: attention of q [B,H,S_q,D] against one K/V chunk
+    [B,H,S_kv,D].  Returns (out f32 [B,H,S_q,D], lse f32 [B,H,S_q])."""
+    lib = _lib.load()
+    B, H, S, D = q.shape
+    if out is None:
+        out = torch.empty(B, H, S, D, device=q.device, dtype=torch.float32)
+    if lse is None:
+        lse = torch.empty(B, H, S, device=q.device, dtype=torch.float32)
+    dq, dk, dv, do, dl = _desc(q), _desc(k), _desc(v), _desc(out), _desc(lse)
+    check(lib.cpattn_partial(dq, dk, dv, _scale(scale), do, dl, _stream_handle(stream)),
+          "cpattn_partial")
+    return out, lse
+
+
+def merge(out_a: torch.Tensor, lse_a: torch.Tensor, out_b: torch.Tensor, lse_b: torch.Tensor,
+          stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """LSE merge of two f32 partials, in place into (out_a, lse_a)."""
+    lib = _lib.load()
+    da, la, db, lb = _desc(out_a), _desc(lse_a), _desc(out_b), _desc(lse_b)
+    check(lib.cpattn_merge(da, la, db, lb, _stream_handle(stream)), "cpattn_merge")
+    return out_a, lse_a
+
+
+def ring_workspace_bytes(q: torch.Tensor, ring_degree: int) -> int:
+    lib = _lib.load()
+    return int(lib.cpattn_ring_workspace_bytes(describe(0, _code(q), q.shape, q.stride()),
+                                               int(ring_degree)))
+
+
+def ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ring_degree: int = 1,
+         ring_anything: bool = False, scale: Optional[float] = None,
+         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+         workspace: Optional[torch.Tensor] = None,
+         stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The ring schedule on one GPU: q [B,H,S_q,D], k, v [B,H,S_kv,D].
+    Returns (out [B,H,S_q,D] in q's dtype, lse f32 [B,H,S_q])."""
+    lib = _lib.load()
+    B, H, S, D = q.shape
+    if out is None:
+        out = torch.empty(B, H, S, D, device=q.device, dtype=q.dtype)
+    if lse is None:
+        lse = torch.empty(B, H, S, device=q.device, dtype=torch.float32)
+    need = ring_workspace_bytes(q, ring_degree)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    dq, dk, dv, do, dl = _desc(q), _desc(k), _desc(v), _desc(out), _desc(lse)
+    check(lib.cpattn_ring(dq, dk, dv, _scale(scale), int(ring_degree), int(bool(ring_anything)),
+                          do, dl, ws_ptr, ws_bytes, _stream_handle(stream)), "cpattn_ring")
+    return out, lse
+
+
+def ulysses_permute(x: torch.Tensor, degree: int, direction: int,
+                    out: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """direction +1: [B,S,H,D] -> [G,B,S,H/G,D]; direction -1: the inverse."""
+    lib = _lib.load()
+    if out is None:
+        if direction == 1:
+            B, S, H, D = x.shape
+            out = torch.empty(degree, B, S, H // max(degree, 1), D, device=x.device, dtype=x.dtype)
+        else:
+            G, B, S, Hg, D = x.shape
+            out = torch.empty(B, S, G * Hg, D, device=x.device, dtype=x.dtype)
+    dx, dy = _desc(x), _desc(out)
+    check(lib.cpattn_ulysses_permute(dx, int(degree), int(direction), dy, _stream_handle(stream)),
+          "cpattn_ulysses_permute")
+    return out
+
+
+def grouped_as_bhsd(t: torch.Tensor) -> torch.Tensor:
+    """[G,B,S,H/G,D] -> strided view [G*B, H/G, S, D] (no copy)."""
+    G, B, S, Hg, D = t.shape
+    return t.view(G * B, S, Hg, D).permute(0, 2, 1, 3)
+
+
+def ulysses_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, degree: int,
+                      scale: Optional[float] = None,
+                      stream: Optional[torch.cuda.Stream] = None,
+                      buffers: Optional[dict] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Ulysses on one GPU: permute q, k, v [B,S,H,D] into G head groups, full
+    attention per group (one launch over all groups), inverse permute of the
+    output.  Returns (out [B,S,H,D], lse f32 [G*B, H/G, S])."""
+    B, S, H, D = q.shape
+    bufs = buffers if buffers is not None else {}
+
+    def buf(name, shape, dtype):
+        t = bufs.get(name)
+        if t is None or tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+            t = torch.empty(shape, device=q.device, dtype=dtype)
+            bufs[name] = t
+        return t
+
+    G = degree
+    qg = ulysses_permute(q, G, 1, out=buf("q", (G, B, S, H // G, D), q.dtype), stream=stream)
+    kg = ulysses_permute(k, G, 1, out=buf("k", (G, B, S, H // G, D), k.dtype), stream=stream)
+    vg = ulysses_permute(v, G, 1, out=buf("v", (G, B, S, H // G, D), v.dtype), stream=stream)
+    og = buf("o", (G, B, S, H // G, D), q.dtype)
+    lse = buf("lse", (G * B, H // G, S), torch.float32)
+    ring(grouped_as_bhsd(qg), grouped_as_bhsd(kg), grouped_as_bhsd(vg), 1, False, scale,
+         out=grouped_as_bhsd(og), lse=lse, stream=stream)
+    out = ulysses_permute(og, G, -1, out=buf("out", (B, S, H, D), q.dtype), stream=stream)
+    return out, lse
+
+
+def last_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word
+    status: 0 = ok, 9 = a kernel-side wait timed out."""
+    return int(_lib.load().cpattn_last_device_status(_stream_handle(stream)))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _lib.load().cpattn_set_wait_timeout_ns(int(ns))
+
+
+__all__ = ["partial", "merge", "ring", "ring_workspace_bytes", "ulysses_permute",
+           "ulysses_attention", "grouped_as_bhsd", "last_device_status", "set_wait_timeout_ns",
+           "CpattnError"]

@@ -1,0 +1,512 @@
+// attn_fwd.cu -- blockwise attention with in-kernel ring schedule for sm_103a.
+//
+// What it computes (page title, section):
+//   Diffusers "Context parallelism", "Ring Attention": every query meets the
+//   K/V block of every ring rank in turn; "Ring Anything Attention": the
+//   blocks may be uneven.  Diffusers "Parallelism" API, ContextParallelConfig
+//   convert_to_fp32: each step's output and LSE are kept in fp32 and merged.
+//   One launch runs the whole ring for a tile of queries: for each chunk c
+//   (in order 0 .. R-1) it computes the chunk's partial output o_c = O_c / l_c
+//   and lse_c = m_c + ln l_c with an online softmax over the chunk's key
+//   tiles, then folds (o_c, lse_c) into the running (o, lse) with
+//     lse = max + log1p(exp(min - max)),  o = e^(lse_r - lse) o_r + e^(lse_c - lse) o_c.
+//   With ring_degree = 1 it is a single partial (cpattn_partial).
+//
+// How (one CTA = two 128-row query tiles of one (batch, head)):
+//   warp 8      TMA producer: Q once, then K_j, V_j tiles (128 keys) through a
+//               STAGES-deep shared-memory ring (128-byte swizzle).
+//   warp 9      MMA issuer (one thread): S_i = Q_i K_j^T into TMEM, then
+//               O_i += P_i V_j with P_i read from TMEM (tcgen05.mma, fp32
+//               accumulation), ping-ponging the two query tiles so the tensor
+//               core works on one tile while the other tile's softmax runs.
+//   warps 0-7   softmax, one warpgroup per query tile, one thread per query
+//               row: S row from TMEM -> row max -> 2^(s*scale*log2e - m)
+//               -> row sum, P (bf16, or fp32 for tf32) back into S's columns;
+//               at each chunk end the normalised partial is merged in fp32
+//               with the running result (held in a global fp32 workspace).
+//   TMEM (512 columns): S_0 | S_1 | O_0 | O_1.
+//   The running max is only raised when it grows by more than 2^8 (exponent
+//   8 in log2 units); between raises P values stay below 256, exact enough
+//   for bf16/fp32 and far from overflow.  The O rescale that a raise needs
+//   happens in TMEM, after the previous P V has completed.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tmem_ops.cuh"
+
+namespace cpattn {
+
+// Device error word: bit flags of waits that ran out of time; read and
+// cleared by the host after a stream synchronisation.
+__device__ unsigned int g_cpattn_device_error = 0;
+
+namespace {
+
+constexpr int kBM = 128;          // query rows per tile (TMEM lanes)
+constexpr int kNT = 2;            // query tiles per CTA
+constexpr int kBN = 128;          // keys per K/V tile
+constexpr int kThreads = 320;     // 8 softmax warps + producer + MMA
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr unsigned kErrWaitProducer = 1u, kErrWaitMma = 2u, kErrWaitSoftmax = 4u;
+
+template <typename T, int D>
+struct Cfg {
+  static constexpr int ES = sizeof(T);
+  static constexpr bool TF32 = (ES == 4);
+  static constexpr int ROW_BYTES = D * ES;
+  static constexpr int NKB = ROW_BYTES / 128;       // 128-byte column blocks per row
+  static constexpr int BOX_COLS = 128 / ES;         // elements per column block
+  static constexpr int Q_TILE_BYTES = kBM * ROW_BYTES;
+  static constexpr int KV_TILE_BYTES = kBN * ROW_BYTES;
+  static constexpr int SMEM_BUDGET = 220 * 1024;
+  static constexpr int STAGES_FIT = (SMEM_BUDGET - kNT * Q_TILE_BYTES) / KV_TILE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int NUM_BARS = 1 + 2 * STAGES + 3 * kNT + 1;
+  static constexpr int SMEM_BYTES =
+      1024 + kNT * Q_TILE_BYTES + STAGES * KV_TILE_BYTES + NUM_BARS * 8 + 16;
+  static constexpr int KSTEP = 32 / ES;             // K elements per MMA (32 bytes)
+  static constexpr int QK_STEPS = ROW_BYTES / 32;
+  static constexpr int PV_STEPS = kBN / KSTEP;
+  static constexpr int P_COLS_PER_STEP = KSTEP * ES / 4;
+  static constexpr uint32_t FMT = TF32 ? 2u : 1u;   // tf32 : bf16
+  static constexpr uint32_t IDESC_QK = make_idesc(FMT, false, kBM, kBN);
+  static constexpr uint32_t IDESC_PV = make_idesc(FMT, true, kBM, D);
+  static constexpr int O_COL = kNT * kBN;
+  static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte blocks");
+  static_assert(O_COL + kNT * D <= (int)kTmemCols, "TMEM budget");
+  static_assert(STAGES >= 2, "need at least two K/V stages");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Walks the (chunk, tile) sequence shared by all roles.
+struct TileWalk {
+  int c = 0, t = 0, nt = 0;
+  __device__ void start(const AttnParams& p) {
+    c = 0;
+    t = 0;
+    nt = ceil_div(p.chunk_start[1] - p.chunk_start[0], kBN);
+  }
+  __device__ void next(const AttnParams& p) {
+    if (++t == nt) {
+      ++c;
+      t = 0;
+      if (c < p.ring_degree) nt = ceil_div(p.chunk_start[c + 1] - p.chunk_start[c], kBN);
+    }
+  }
+};
+
+// Multiplies this thread's O row (TMEM) by `factor`.
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t tO, float factor) {
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t o[32];
+    tmem_ld_x32(tO + c0, o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * factor);
+    tmem_st_x32(tO + c0, o);
+  }
+  tmem_wait_st();
+}
+
+// End of chunk c for this thread's query row: emit the chunk's partial
+// (o_c = O / l, lse_c = m ln2 + ln l) and fold it into the running result.
+template <typename T, int D>
+__device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO, int c,
+                                               float m_used, float l, int b, int h, int q_row,
+                                               bool row_ok) {
+  const bool last = (c == p.ring_degree - 1);
+  const float inv_l = 1.0f / l;
+  const float lse_c = (m_used + log2f(l)) * kLn2;
+  const int64_t flat = (static_cast<int64_t>(b) * p.heads + h) * p.s_q + q_row;
+  float w_run = 0.f, w_c = 1.f, lse_new = lse_c;
+  if (c > 0 && row_ok) {
+    const float lse_run = p.ws_lse[flat];
+    const float hi = fmaxf(lse_run, lse_c), lo = fminf(lse_run, lse_c);
+    lse_new = hi + log1pf(expf(lo - hi));
+    w_run = expf(lse_run - lse_new);
+    w_c = expf(lse_c - lse_new);
+  }
+  float* ws_row = p.ws_o + flat * D;
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t o[32];
+    __syncwarp();
+    tmem_ld_x32(tO + c0, o);
+    if (row_ok) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = u2f(o[i]) * inv_l;   // partial output o_c
+      if (c > 0) {
+        const float4* src = reinterpret_cast<const float4*>(ws_row + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 r = src[i];
+          v[4 * i + 0] = w_run * r.x + w_c * v[4 * i + 0];
+          v[4 * i + 1] = w_run * r.y + w_c * v[4 * i + 1];
+          v[4 * i + 2] = w_run * r.z + w_c * v[4 * i + 2];
+          v[4 * i + 3] = w_run * r.w + w_c * v[4 * i + 3];
+        }
+      }
+      if (!last) {
+        float4* dst = reinterpret_cast<float4*>(ws_row + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      } else if (p.out_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + b * p.out_sb +
+                                                h * p.out_sh + q_row * p.out_ss + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + b * p.out_sb +
+                                              h * p.out_sh + q_row * p.out_ss + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]),
+                              pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                              pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                              pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+      }
+    }
+  }
+  if (row_ok) {
+    if (last)
+      p.lse[b * p.lse_sb + h * p.lse_sh + q_row * p.lse_ss] = lse_new;
+    else
+      p.ws_lse[flat] = lse_new;
+  }
+  __syncwarp();
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ AttnParams p) {
+  using C = Cfg<T, D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+
+  const uint32_t sQ = smem_addr(smem);
+  const uint32_t sKV = sQ + kNT * C::Q_TILE_BYTES;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + kNT * C::Q_TILE_BYTES + C::STAGES * C::KV_TILE_BYTES);
+  const uint32_t bar0 = smem_addr(bars);
+  const uint32_t BAR_Q = bar0;
+  auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
+  auto bar_s = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + i); };
+  auto bar_p = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + kNT + i); };
+  auto bar_o = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + 2 * kNT + i); };
+  const uint32_t BAR_DRAIN = bar0 + 8u * (1 + 2 * C::STAGES + 3 * kNT);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int q_row0 = blockIdx.x * (kNT * kBM);
+  const int h = blockIdx.y, b = blockIdx.z;
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR_Q, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int i = 0; i < kNT; ++i) {
+      mbar_init(bar_s(i), 1);
+      mbar_init(bar_p(i), 4);   // one arrival per softmax warp
+      mbar_init(bar_o(i), 1);
+    }
+    mbar_init(BAR_DRAIN, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(smem_addr(tmem_holder), kTmemCols);
+  if (warp == kWarpProducer && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  int n_tiles = 0;
+  for (int c = 0; c < p.ring_degree; ++c)
+    n_tiles += ceil_div(p.chunk_start[c + 1] - p.chunk_start[c], kBN);
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(BAR_Q, kNT * C::Q_TILE_BYTES);
+      for (int i = 0; i < kNT; ++i)
+        for (int kb = 0; kb < C::NKB; ++kb)
+          tma_load_4d(sQ + i * C::Q_TILE_BYTES + kb * kBM * 128, &tm_q, BAR_Q, kb * C::BOX_COLS,
+                      q_row0 + i * kBM, h, b);
+      int ld = 0;
+      bool ok = true;
+      TileWalk w;
+      w.start(p);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int key0 = p.chunk_start[w.c] + w.t * kBN;
+        for (int which = 0; which < 2; ++which) {
+          const int s = ld % C::STAGES;
+          const uint32_t ph = (ld / C::STAGES) & 1;
+          ok = mbar_wait(bar_empty(s), ph ^ 1, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitProducer);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar_full(s), C::KV_TILE_BYTES);
+          const CUtensorMap* tm = which == 0 ? &tm_k : &tm_v;
+          for (int kb = 0; kb < C::NKB; ++kb)
+            tma_load_4d(sKV + s * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar_full(s),
+                        kb * C::BOX_COLS, key0, h, b);
+          ++ld;
+        }
+        w.next(p);
+      }
+      if (!ok) {
+        // leave no copy in flight into this CTA's shared memory
+        mbar_drain(BAR_Q, 0, p.timeout_ns);
+        for (int x = ld > C::STAGES ? ld - C::STAGES : 0; x < ld; ++x)
+          mbar_drain(bar_full(x % C::STAGES), (x / C::STAGES) & 1, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      auto issue_qk = [&](int i, int stage) {
+        const uint32_t d_tmem = tmem + i * kBN;
+        const uint32_t a_base = sQ + i * C::Q_TILE_BYTES;
+        const uint32_t b_base = sKV + stage * C::KV_TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+          const uint32_t off_a = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
+          const uint32_t off_b = (kk / 4) * (kBN * 128) + (kk % 4) * 32;
+          mma_ss<C::TF32>(d_tmem, smem_desc_sw128(a_base + off_a, 16, 1024),
+                          smem_desc_sw128(b_base + off_b, 16, 1024), C::IDESC_QK, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int i, int stage, uint32_t acc) {
+        const uint32_t d_tmem = tmem + C::O_COL + i * D;
+        const uint32_t a_tmem = tmem + i * kBN;
+        const uint32_t b_base = sKV + stage * C::KV_TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+          mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_STEP,
+                          smem_desc_sw128(b_base + kk * C::KSTEP * 128, kBN * 128, 1024),
+                          C::IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(BAR_Q, 0, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
+      if (ok) ok = mbar_wait(bar_full(0), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0, 0);
+        mma_commit(bar_s(0));
+        issue_qk(1, 0);
+        mma_commit(bar_s(1));
+        mma_commit(bar_empty(0));
+      }
+      TileWalk w;
+      w.start(p);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const uint32_t acc = w.t != 0 ? 1u : 0u;
+        const int lv = 2 * j + 1, sv = lv % C::STAGES;
+        const uint32_t phv = (lv / C::STAGES) & 1;
+        const int lk = 2 * j + 2, sk = lk % C::STAGES;
+        const uint32_t phk = (lk / C::STAGES) & 1;
+        const bool more = j + 1 < n_tiles;
+        // query tile 0
+        ok = mbar_wait(bar_p(0), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
+        if (ok) ok = mbar_wait(bar_full(sv), phv, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(0, sv, acc);
+        if (more) {
+          ok = mbar_wait(bar_full(sk), phk, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(0, sk);
+          mma_commit(bar_s(0));
+        } else {
+          mma_commit(bar_o(0));
+        }
+        // query tile 1
+        ok = mbar_wait(bar_p(1), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(1, sv, acc);
+        mma_commit(bar_empty(sv));
+        if (more) {
+          issue_qk(1, sk);
+          mma_commit(bar_s(1));
+          mma_commit(bar_empty(sk));
+        } else {
+          mma_commit(bar_o(1));
+        }
+        w.next(p);
+      }
+      if (!ok) {
+        // let every MMA already issued finish before TMEM is released
+        mma_commit(BAR_DRAIN);
+        mbar_drain(BAR_DRAIN, 0, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int wg = warp / 4;
+    const int quarter = warp % 4;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + wg * kBN;
+    const uint32_t tO = tmem + lane_base + C::O_COL + wg * D;
+    const int q_row = q_row0 + wg * kBM + quarter * 32 + lane;
+    const bool row_ok = q_row < p.s_q;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    TileWalk w;
+    w.start(p);
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = mbar_wait(bar_s(wg), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      if (w.t == 0 && w.c > 0)
+        chunk_epilogue<T, D>(p, tO, w.c - 1, m_used, l, b, h, q_row, row_ok);
+
+      uint32_t s[kBN];
+      tmem_ld_x128(tS, s);
+      const int valid = p.chunk_start[w.c + 1] - (p.chunk_start[w.c] + w.t * kBN);
+      if (valid < kBN) {
+#pragma unroll
+        for (int i = 0; i < kBN; ++i)
+          if (i >= valid) s[i] = f2u(-INFINITY);
+      }
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = u2f(s[k]);
+#pragma unroll
+      for (int i = 8; i < kBN; ++i) mx[i % 8] = fmaxf(mx[i % 8], u2f(s[i]));
+      const float row_max =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_tile = row_max * sl2;
+      float factor = 1.f;
+      bool need = false;
+      if (w.t == 0) {
+        m_used = m_tile;
+        l = 0.f;
+      } else if (m_tile > m_used + kRescaleThreshold) {
+        factor = ex2_approx(m_used - m_tile);
+        m_used = m_tile;
+        l *= factor;
+        need = true;
+      }
+      if (__any_sync(0xffffffffu, need)) rescale_o<D>(tO, factor);
+
+      const float neg_m = -m_used;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (!C::TF32) {
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int i = 0; i < kBN / 2; ++i) {
+          const float e0 = ex2_approx(fmaf(u2f(s[2 * i]), sl2, neg_m));
+          const float e1 = ex2_approx(fmaf(u2f(s[2 * i + 1]), sl2, neg_m));
+          acc[i % 4] += e0 + e1;
+          pk[i] = pack_bf16x2(e0, e1);
+        }
+        tmem_st_x64(tS, pk);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) {
+          const float e = ex2_approx(fmaf(u2f(s[i]), sl2, neg_m));
+          acc[i % 4] += e;
+          s[i] = f2u(e);
+        }
+        tmem_st_x128(tS, s);
+      }
+      l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p(wg));
+      w.next(p);
+    }
+    if (ok) {
+      ok = mbar_wait(bar_o(wg), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        chunk_epilogue<T, D>(p, tO, p.ring_degree - 1, m_used, l, b, h, q_row, row_ok);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                        const AttnParams& p, cudaStream_t stream) {
+  using C = Cfg<T, D>;
+  auto kernel = attn_fwd_kernel<T, D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((p.s_q + kNT * kBM - 1) / (kNT * kBM), p.heads, p.batch);
+  kernel<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(InDtype dt, int head_dim, const CUtensorMap& tm_q,
+                             const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                             const AttnParams& p, cudaStream_t stream) {
+  if (dt == InDtype::BF16 && head_dim == 128)
+    return launch_impl<__nv_bfloat16, 128>(tm_q, tm_k, tm_v, p, stream);
+  if (dt == InDtype::BF16 && head_dim == 64)
+    return launch_impl<__nv_bfloat16, 64>(tm_q, tm_k, tm_v, p, stream);
+  if (dt == InDtype::F32 && head_dim == 64)
+    return launch_impl<float, 64>(tm_q, tm_k, tm_v, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_clear_device_error(unsigned int* value, cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(value, g_cpattn_device_error, sizeof(unsigned int));
+  if (e != cudaSuccess || *value == 0) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_cpattn_device_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace cpattn

@@ -1,0 +1,61 @@
+// internal.h -- declarations shared by the translation units of libcpattn.so
+// (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/cpattn.h"
+
+namespace cpattn {
+
+// Parameters of one attention launch (ring or single partial).
+struct AttnParams {
+  void* out;             // [B, H, S_q, D], f32 or the input dtype
+  int64_t out_sb, out_sh, out_ss;
+  float* lse;            // [B, H, S_q] f32
+  int64_t lse_sb, lse_sh, lse_ss;
+  float* ws_o;           // running merged output, f32 [B*H*S_q, D]  (ring_degree > 1)
+  float* ws_lse;         // running merged LSE, f32 [B*H*S_q]        (ring_degree > 1)
+  int batch, heads, s_q, s_kv;
+  float scale_log2;      // softmax scale times log2(e)
+  int ring_degree;
+  int out_f32;           // 1: out is f32, 0: out has the input dtype (bf16)
+  unsigned long long timeout_ns;
+  int chunk_start[CPATTN_MAX_RING_DEGREE + 1];
+};
+
+enum class InDtype { F32, BF16 };
+
+// Launches the attention kernel; tensor maps already encoded.
+cudaError_t launch_attention(InDtype dt, int head_dim, const CUtensorMap& tm_q,
+                             const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                             const AttnParams& p, cudaStream_t stream);
+
+struct MergeParams {
+  float* o_a;
+  float* l_a;
+  const float* o_b;
+  const float* l_b;
+  int64_t rows;          // B * H * S
+  int head_dim;
+  int heads, seq;        // for the strided index map
+  int64_t oa_s[3], ob_s[3], la_s[3], lb_s[3];   // strides (b, h, s) in elements
+  int dense;             // 1: all four tensors are dense row-major
+};
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+
+struct PermuteParams {
+  const void* x;
+  void* y;
+  int64_t batch, seq, heads, head_dim, degree;
+  int dir;               // +1 forward, -1 inverse
+  int elem_bytes;
+};
+cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream);
+
+// Error word helpers (defined with the device symbol).
+cudaError_t read_and_clear_device_error(unsigned int* value, cudaStream_t stream);
+
+}  // namespace cpattn

@@ -1,0 +1,173 @@
+// merge_permute.cu -- the two HBM-bound steps of the hot path.
+//
+// merge: LSE merge of two fp32 partials, in place into (o_a, lse_a)
+//   (Diffusers "Parallelism" API, ContextParallelConfig convert_to_fp32:
+//   output and LSE converted to fp32 "for ring attention numerical
+//   stability"; the formula follows from the definition of LSE):
+//     lse = max(a, b) + log1p(exp(min(a, b) - max(a, b)))
+//     o   = exp(a - lse) o_a + exp(b - lse) o_b,   (0, -inf) if both empty.
+//   One thread per 16-byte vector of a row; the D/4 threads of a row sit in
+//   one warp, read both LSEs, synchronise, then one of them writes lse_a.
+//
+// permute: the Ulysses head regroup (Diffusers "Context parallelism",
+//   "Ulysses Attention") as a layout copy between [B, S, H, D] and
+//   [G, B, S, H/G, D].  Every (b, s, g) segment of H/G * D elements is
+//   contiguous on both sides; threads walk the destination in order with
+//   16-byte vectors (4 in flight per thread), or element by element when a
+//   segment is not a whole number of vectors.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr int kMergeThreads = 256;
+constexpr int kPermuteThreads = 256;
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+  const int vpr = p.head_dim / 4;                          // float4 per row
+  const int64_t total = p.rows * vpr;
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+       base < total; base += stride) {
+    const int64_t i = base + lane;
+    const bool in = i < total;
+    const int64_t r = in ? i / vpr : 0;
+    const int cv = static_cast<int>(i - r * vpr);
+    int64_t oa, ob, la, lb;
+    if (p.dense) {
+      oa = ob = r * p.head_dim + 4 * cv;
+      la = lb = r;
+    } else {
+      const int64_t s = r % p.seq, bh = r / p.seq;
+      const int64_t hh = bh % p.heads, bb = bh / p.heads;
+      oa = bb * p.oa_s[0] + hh * p.oa_s[1] + s * p.oa_s[2] + 4 * cv;
+      ob = bb * p.ob_s[0] + hh * p.ob_s[1] + s * p.ob_s[2] + 4 * cv;
+      la = bb * p.la_s[0] + hh * p.la_s[1] + s * p.la_s[2];
+      lb = bb * p.lb_s[0] + hh * p.lb_s[1] + s * p.lb_s[2];
+    }
+    float a = 0.f, b = 0.f;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+    if (in) {
+      a = p.l_a[la];
+      b = p.l_b[lb];
+      x = *reinterpret_cast<const float4*>(p.o_a + oa);
+      y = __ldcs(reinterpret_cast<const float4*>(p.o_b + ob));
+    }
+    __syncwarp();   // every lane of the row has read lse_a before it is overwritten
+    if (in) {
+      float lse, wa, wb;
+      if (a == -INFINITY && b == -INFINITY) {
+        lse = -INFINITY;
+        wa = wb = 0.f;
+      } else {
+        const float hi = fmaxf(a, b), lo = fminf(a, b);
+        lse = hi + log1pf(expf(lo - hi));
+        wa = expf(a - lse);
+        wb = expf(b - lse);
+      }
+      const float4 o = make_float4(wa * x.x + wb * y.x, wa * x.y + wb * y.y,
+                                   wa * x.z + wb * y.z, wa * x.w + wb * y.w);
+      __stcs(reinterpret_cast<float4*>(p.o_a + oa), o);
+      if (cv == 0) p.l_a[la] = lse;
+    }
+  }
+}
+
+// Destination index -> source index of the same element (or vector).
+//   unit: elements (or 16-byte vectors) per (b, s, g) segment.
+//   dir +1: destination [G][B*S][unit], source [B*S][G][unit]
+//   dir -1: destination [B*S][G][unit], source [G][B*S][unit]
+template <typename Index>
+__device__ __forceinline__ Index source_of(Index idx, Index unit, Index bs, Index g, int dir) {
+  const Index w = idx % unit, seg = idx / unit;
+  Index src_seg;
+  if (dir > 0)
+    src_seg = (seg % bs) * g + seg / bs;
+  else
+    src_seg = (seg % g) * bs + seg / g;
+  return src_seg * unit + w;
+}
+
+template <typename V, typename Index>
+__global__ void __launch_bounds__(kPermuteThreads)
+    permute_kernel(const V* __restrict__ x, V* __restrict__ y, Index total, Index unit, Index bs,
+                   Index g, int dir) {
+  const Index stride = static_cast<Index>(gridDim.x) * blockDim.x;
+  for (Index base = static_cast<Index>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+       base += stride * kUnroll) {
+    V v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const Index idx = base + u * stride;
+      if (idx < total) v[u] = __ldcs(x + source_of<Index>(idx, unit, bs, g, dir));
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const Index idx = base + u * stride;
+      if (idx < total) __stcs(y + idx, v[u]);
+    }
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+template <typename V>
+cudaError_t launch_permute_typed(const PermuteParams& p, int64_t total, int64_t unit,
+                                 cudaStream_t stream) {
+  const int64_t bs = p.batch * p.seq;
+  const int64_t want = (total + kPermuteThreads * kUnroll - 1) / (kPermuteThreads * kUnroll);
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  const int blocks = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+  const V* x = static_cast<const V*>(p.x);
+  V* y = static_cast<V*>(p.y);
+  if (total + static_cast<int64_t>(blocks) * kPermuteThreads * kUnroll < (int64_t(1) << 31))
+    permute_kernel<V, uint32_t><<<blocks, kPermuteThreads, 0, stream>>>(
+        x, y, static_cast<uint32_t>(total), static_cast<uint32_t>(unit),
+        static_cast<uint32_t>(bs), static_cast<uint32_t>(p.degree), p.dir);
+  else
+    permute_kernel<V, uint64_t><<<blocks, kPermuteThreads, 0, stream>>>(
+        x, y, static_cast<uint64_t>(total), static_cast<uint64_t>(unit),
+        static_cast<uint64_t>(bs), static_cast<uint64_t>(p.degree), p.dir);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+  const int64_t total = p.rows * (p.head_dim / 4);
+  if (total == 0) return cudaSuccess;
+  const int64_t want = (total + kMergeThreads - 1) / kMergeThreads;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  const int blocks = static_cast<int>(want < cap ? want : cap);
+  merge_kernel<<<blocks, kMergeThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream) {
+  const int64_t seg_elems = (p.heads / p.degree) * p.head_dim;
+  const int64_t total_elems = p.batch * p.seq * p.heads * p.head_dim;
+  if (total_elems == 0) return cudaSuccess;
+  const int64_t seg_bytes = seg_elems * p.elem_bytes;
+  const bool vec = seg_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(p.x) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(p.y) % 16 == 0;
+  if (vec)
+    return launch_permute_typed<uint4>(p, total_elems * p.elem_bytes / 16, seg_bytes / 16, stream);
+  if (p.elem_bytes == 2)
+    return launch_permute_typed<unsigned short>(p, total_elems, seg_elems, stream);
+  if (p.elem_bytes == 4)
+    return launch_permute_typed<unsigned int>(p, total_elems, seg_elems, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cpattn

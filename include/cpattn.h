@@ -1,0 +1,172 @@
+/*
+ * cpattn.h -- C ABI of libcpattn.so: the data-parallel hot path of
+ * context-parallel attention (Ring, Ring Anything and Ulysses) on one GB300.
+ *
+ * Sources (page title, section):
+ *   [CP]   Diffusers "Context parallelism" guide: variants table, "Ring
+ *          Attention", "Ulysses Attention", "Ring Anything Attention".
+ *   [API]  Diffusers "Parallelism" API page, ContextParallelConfig:
+ *          ring_degree, ulysses_degree, convert_to_fp32, ring_anything.
+ *   [PARA] ParaAttention README, "Run Unified Attention ... with
+ *          torch.compile": scaled_dot_product_attention with no mask, no
+ *          dropout, not causal, on [B, H, S, D] tensors chunked on dim -2.
+ *   [CFG]  diffusers _modeling_parallel.py, ContextParallelConfig
+ *          (__post_init__ validation).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Tensors are described by cpattn_tensor: a DEVICE pointer, a dtype, and
+ *   shape/stride in ELEMENTS.  The innermost dimension must have stride 1;
+ *   every other stride times the element size must be a multiple of 16 bytes,
+ *   and the data pointer must be 16-byte aligned (CPATTN_ERR_LAYOUT).
+ * - Ownership: the caller allocates every input, output and workspace buffer
+ *   and keeps it alive until the stream has finished the call.  The library
+ *   allocates no device memory and keeps no state between calls except one
+ *   device error word (see cpattn_last_device_status).  Descriptors are only
+ *   read during the call.
+ * - Asynchrony: every call is enqueued on `stream` (a cudaStream_t; NULL is the
+ *   legacy default stream).  Argument errors are returned synchronously before
+ *   anything is launched; a launch failure returns CPATTN_ERR_CUDA.  A wait
+ *   inside a kernel that runs out of its time limit records CPATTN_ERR_TIMEOUT
+ *   in the device error word, and the kernel returns.
+ * - Scale: scale <= 0 or NaN selects 1/sqrt(D), the scaled_dot_product_attention
+ *   default [PARA].
+ * - Supported: bf16 inputs with D in {64, 128} (tensor cores, bf16 operands,
+ *   fp32 accumulation) and fp32 inputs with D = 64 (tensor cores, tf32
+ *   operands, fp32 accumulation).  Anything else: CPATTN_ERR_UNSUPPORTED.
+ *   There is no CPU fallback.
+ */
+#ifndef CPATTN_H_
+#define CPATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CPATTN_OK = 0,
+  CPATTN_ERR_NULL = 1,          /* a required pointer is NULL */
+  CPATTN_ERR_DTYPE = 2,         /* dtype not allowed for that argument */
+  CPATTN_ERR_SHAPE = 3,         /* ranks or extents inconsistent */
+  CPATTN_ERR_DIVISIBILITY = 4,  /* S % ring_degree or H % degree != 0 */
+  CPATTN_ERR_LAYOUT = 5,        /* inner stride != 1, or not 16-byte aligned */
+  CPATTN_ERR_UNSUPPORTED = 6,   /* valid, but outside what the kernels cover */
+  CPATTN_ERR_WORKSPACE = 7,     /* workspace missing or too small */
+  CPATTN_ERR_CUDA = 8,          /* a CUDA runtime call failed */
+  CPATTN_ERR_TIMEOUT = 9        /* a device-side wait ran out of time */
+} cpattn_status;
+
+typedef enum { CPATTN_F32 = 0, CPATTN_BF16 = 1 } cpattn_dtype;
+
+#define CPATTN_MAX_DIMS 5
+#define CPATTN_MAX_RING_DEGREE 64
+
+typedef struct {
+  void* data;                        /* device pointer */
+  int32_t dtype;                     /* cpattn_dtype */
+  int32_t ndim;
+  int64_t shape[CPATTN_MAX_DIMS];    /* elements */
+  int64_t stride[CPATTN_MAX_DIMS];   /* elements */
+} cpattn_tensor;
+
+/*
+ * cpattn_partial -- one ring step: attention of a query chunk against ONE K/V
+ * chunk, emitting the partial output and its log-sum-exp ([CP] "Ring
+ * Attention": each GPU computes attention against the K/V block it holds;
+ * [API] convert_to_fp32: output and LSE kept in float32).
+ *   q   [B, H, S_q, D]   bf16 or f32
+ *   k,v [B, H, S_kv, D]  same dtype as q, S_kv >= 1
+ *   out [B, H, S_q, D]   f32 (written):  softmax(scale q k^T) v
+ *   lse [B, H, S_q]      f32 (written):  natural log of sum_j exp(scale q.k_j)
+ * S_q = 0 (or B = 0, H = 0) is a no-op.  S_kv = 0 is CPATTN_ERR_SHAPE.
+ */
+cpattn_status cpattn_partial(const cpattn_tensor* q, const cpattn_tensor* k,
+                             const cpattn_tensor* v, float scale,
+                             cpattn_tensor* out, cpattn_tensor* lse,
+                             void* stream);
+
+/*
+ * cpattn_merge -- LSE merge of two partials over disjoint key sets, in place
+ * into (out_a, lse_a) ([API] convert_to_fp32, "for ring attention numerical
+ * stability"):
+ *   lse = max(a, b) + log1p(exp(min(a, b) - max(a, b)))
+ *   out = exp(a - lse) out_a + exp(b - lse) out_b
+ * lse = -inf marks an empty partial; two empty partials give (0, -inf).
+ *   out_a, out_b [B, H, S, D] f32;  lse_a, lse_b [B, H, S] f32.
+ * out_a/lse_a may not overlap out_b/lse_b.
+ */
+cpattn_status cpattn_merge(cpattn_tensor* out_a, cpattn_tensor* lse_a,
+                           const cpattn_tensor* out_b,
+                           const cpattn_tensor* lse_b, void* stream);
+
+/*
+ * cpattn_ring_workspace_bytes -- bytes of device workspace cpattn_ring needs
+ * for q [B, H, S_q, D] and this ring_degree: the running merged output
+ * (f32 [B, H, S_q, D]) and its LSE (f32 [B, H, S_q]); 0 when ring_degree = 1.
+ * Returns 0 for an invalid descriptor.
+ */
+size_t cpattn_ring_workspace_bytes(const cpattn_tensor* q, int ring_degree);
+
+/*
+ * cpattn_ring -- the whole ring schedule simulated on one GPU ([CP] "Ring
+ * Attention"): the keys are split into ring_degree chunks; every query tile
+ * meets every chunk in order 0 .. R-1, each meeting emits (partial out, f32
+ * LSE) and the partials are folded with the merge above.  All chunk loops and
+ * merges run inside one kernel launch.
+ *   ring_anything = 0: S_kv % ring_degree != 0 is CPATTN_ERR_DIVISIBILITY
+ *     ([CP] variants table).
+ *   ring_anything = 1: any S_kv >= ring_degree; the first S_kv % R chunks are
+ *     one key longer ([CP] "Ring Anything Attention"; no mask exists here,
+ *     as that variant requires).
+ *   q [B, H, S_q, D], k, v [B, H, S_kv, D]: bf16, or f32 with D = 64.
+ *   out [B, H, S_q, D] same dtype as q (written); lse [B, H, S_q] f32.
+ *   workspace: device buffer of at least cpattn_ring_workspace_bytes (16-byte
+ *     aligned), may be NULL when ring_degree = 1; its contents on entry do
+ *     not matter.
+ *   1 <= ring_degree <= CPATTN_MAX_RING_DEGREE.
+ */
+cpattn_status cpattn_ring(const cpattn_tensor* q, const cpattn_tensor* k,
+                          const cpattn_tensor* v, float scale, int ring_degree,
+                          int ring_anything, cpattn_tensor* out,
+                          cpattn_tensor* lse, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
+ * cpattn_ulysses_permute -- the Ulysses head regroup ([CP] "Ulysses
+ * Attention": the all-to-all leaves each of G ranks every token for H/G
+ * heads), on one GPU a bit-exact layout permute:
+ *   dir = +1: x [B, S, H, D] -> y [G, B, S, H/G, D],
+ *             y[g, b, s, hh, :] = x[b, s, g*H/G + hh, :]
+ *   dir = -1: x [G, B, S, H/G, D] -> y [B, S, H, D] (the inverse map)
+ * degree = G >= 1 with H % G == 0 (else CPATTN_ERR_DIVISIBILITY).  Any dtype
+ * of this header (the copy moves bytes).  x and y must be contiguous and must
+ * not overlap.
+ */
+cpattn_status cpattn_ulysses_permute(const cpattn_tensor* x, int degree,
+                                     int dir, cpattn_tensor* y, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* cpattn_status_string(cpattn_status status);
+
+/*
+ * cpattn_last_device_status -- synchronises `stream`, then reads and clears
+ * the device error word that kernel-side waits set when they time out.
+ * Returns CPATTN_OK, CPATTN_ERR_TIMEOUT, or CPATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+cpattn_status cpattn_last_device_status(void* stream);
+
+/*
+ * cpattn_set_wait_timeout_ns -- time limit of every kernel-side wait on an
+ * mbarrier (default 2e9 ns).  Process-wide, read at each launch.
+ */
+void cpattn_set_wait_timeout_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H_ */

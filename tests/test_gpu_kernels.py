@@ -1,0 +1,239 @@
+"""GPU parity of every kernel against the fp64 oracle on seeded inputs, at
+sizes the oracle finishes in seconds that still span several tiles and a
+ragged tail, plus the degenerate cases.
+
+Tolerances: bf16 inputs -> output max-abs 1e-2, LSE max-abs 1e-3 (N(0,1)
+inputs); fp32 inputs (tf32 tensor cores) -> output 2e-3, LSE 1e-3; the merge
+(pure fp32 arithmetic) -> 2e-5 relative to the magnitudes involved; the
+permute -> bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import context_attention_partial_gb300 as cp
+import oracle
+from context_attention_partial_gb300.workloads import make_partials, make_qkv
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = {torch.bfloat16: (1e-2, 1e-3), torch.float32: (2e-3, 1e-3)}
+
+
+def maxabs(a, b):
+    a = a.detach().float().cpu().numpy() if hasattr(a, "detach") else np.asarray(a)
+    return float(np.max(np.abs(a - b))) if np.size(b) else 0.0
+
+
+def status_ok():
+    assert cp.last_device_status() == 0
+
+
+# ----------------------------------------------------------------------------
+# Ulysses permute: bit-exact
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("shape,g,dtype", [
+    ((1, 4608, 24, 128), 4, torch.bfloat16),      # the Ulysses workload's tensors
+    ((2, 37, 12, 64), 3, torch.bfloat16),
+    ((1, 5, 6, 8), 2, torch.float32),
+    ((2, 3, 10, 3), 5, torch.bfloat16),           # 12-byte segments: element path
+    ((1, 9, 7, 5), 7, torch.float32),             # 20-byte segments
+    ((2, 17, 8, 128), 1, torch.bfloat16),         # G = 1 is the identity layout
+])
+def test_permute_bit_exact(shape, g, dtype):
+    x = make_qkv(shape, dtype, seed=3)[0]
+    y = cp.ulysses_permute(x.to(DEV), g, 1)
+    torch.cuda.synchronize()
+    ref = oracle.ulysses_permute(x, g, 1)
+    assert tuple(y.shape) == tuple(ref.shape)
+    assert torch.equal(y.cpu(), ref)
+    back = cp.ulysses_permute(y, g, -1)
+    torch.cuda.synchronize()
+    assert torch.equal(back.cpu(), x)
+    assert torch.equal(back.cpu(), oracle.ulysses_permute(ref, g, -1))
+
+
+def test_permute_rejects_indivisible_heads():
+    x = torch.zeros(1, 4, 6, 8, device=DEV, dtype=torch.bfloat16)
+    with pytest.raises(cp.CpattnError) as e:
+        cp.ulysses_permute(x, 4, 1, out=torch.zeros(4, 1, 4, 1, 8, device=DEV, dtype=torch.bfloat16))
+    assert e.value.name == "CPATTN_ERR_DIVISIBILITY"
+
+
+# ----------------------------------------------------------------------------
+# merge
+# ----------------------------------------------------------------------------
+def _merge_check(o_a, l_a, o_b, l_b, ga, gla):
+    ro, rl = oracle.merge(o_a, l_a, o_b, l_b)
+    scale = max(1.0, float(np.abs(o_a.numpy()).max()), float(np.abs(o_b.numpy()).max()))
+    assert maxabs(ga, ro) <= 2e-5 * scale
+    fin = np.isfinite(rl)
+    g = gla.cpu().numpy()
+    assert np.array_equal(np.isfinite(g), fin)
+    assert np.max(np.abs(g[fin] - rl[fin]), initial=0.0) <= 2e-5 * max(1.0, np.abs(rl[fin]).max())
+    assert np.all(g[~fin] == -np.inf)
+
+
+@pytest.mark.parametrize("shape", [(1, 24, 4608, 128), (2, 3, 77, 64), (1, 1, 5, 4)])
+def test_merge_matches_oracle(shape):
+    o_a, l_a, o_b, l_b = make_partials(shape[:3], shape[3], seed=5)
+    # empty partials: one side, the other side, both sides
+    l_a[..., 0] = -math.inf
+    if shape[2] > 2:
+        l_b[..., 1] = -math.inf
+        l_a[..., 2] = -math.inf
+        l_b[..., 2] = -math.inf
+        o_a[..., 2, :] = 0
+        o_b[..., 2, :] = 0
+    o_a[..., 0, :] = 0
+    ga, gla = o_a.to(DEV), l_a.to(DEV)
+    cp.merge(ga, gla, o_b.to(DEV), l_b.to(DEV))
+    torch.cuda.synchronize()
+    _merge_check(o_a, l_a, o_b, l_b, ga, gla)
+
+
+def test_merge_strided_views():
+    o_a, l_a, o_b, l_b = make_partials((2, 3, 40), 64, seed=6)
+    big = torch.zeros(2, 3, 50, 64)
+    big[:, :, 5:45] = o_a
+    gbig = big.to(DEV)
+    ga = gbig[:, :, 5:45]
+    glbig = torch.zeros(2, 3, 50).to(DEV)
+    glbig[:, :, 5:45] = l_a.to(DEV)
+    gla = glbig[:, :, 5:45]
+    cp.merge(ga, gla, o_b.to(DEV), l_b.to(DEV))
+    torch.cuda.synchronize()
+    _merge_check(o_a, l_a, o_b, l_b, ga, gla)
+    assert torch.all(gbig[:, :, :5] == 0) and torch.all(gbig[:, :, 45:] == 0)
+
+
+def test_merge_identity_and_self():
+    o_a, l_a, _, _ = make_partials((1, 2, 33), 128, seed=7)
+    ga, gla = o_a.to(DEV), l_a.to(DEV)
+    cp.merge(ga, gla, torch.zeros_like(ga), torch.full_like(gla, -math.inf))
+    torch.cuda.synchronize()
+    assert torch.equal(ga.cpu(), o_a) and torch.equal(gla.cpu(), l_a)
+    cp.merge(ga, gla, o_a.to(DEV), l_a.to(DEV))
+    torch.cuda.synchronize()
+    assert maxabs(ga, o_a.numpy()) <= 1e-6 * 4
+    assert maxabs(gla, l_a.numpy() + math.log(2)) <= 1e-5
+
+
+# ----------------------------------------------------------------------------
+# partial (one chunk) and ring (chunk loop + merges in one kernel)
+# ----------------------------------------------------------------------------
+PARTIAL_CASES = [
+    # (B, H, S_q, S_kv, D, dtype)
+    (1, 2, 300, 333, 128, torch.bfloat16),
+    (2, 3, 1, 1, 128, torch.bfloat16),
+    (1, 2, 256, 128, 128, torch.bfloat16),
+    (1, 1, 513, 700, 64, torch.bfloat16),
+    (1, 2, 200, 257, 64, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", PARTIAL_CASES, ids=lambda c: "x".join(map(str, c[:5])) + str(c[5])[-4:])
+def test_partial_matches_oracle(case):
+    B, H, Sq, Skv, D, dt = case
+    g = torch.Generator("cpu").manual_seed(11)
+    q = torch.randn(B, H, Sq, D, generator=g).to(dt)
+    k = torch.randn(B, H, Skv, D, generator=g).to(dt)
+    v = torch.randn(B, H, Skv, D, generator=g).to(dt)
+    out, lse = cp.partial(q.to(DEV), k.to(DEV), v.to(DEV))
+    torch.cuda.synchronize()
+    status_ok()
+    ro, rl = oracle.partial(q, k, v, D ** -0.5)
+    to, tl = TOL[dt]
+    assert out.dtype == torch.float32
+    assert maxabs(out, ro) <= to
+    assert maxabs(lse, rl) <= tl
+
+
+RING_CASES = [
+    # (B, H, S_q, S_kv, D, dtype, R, anything)
+    (1, 2, 300, 300, 128, torch.bfloat16, 3, False),
+    (1, 2, 300, 301, 128, torch.bfloat16, 3, True),      # 101/100/100
+    (2, 2, 129, 1000, 128, torch.bfloat16, 5, False),
+    (1, 3, 256, 256, 64, torch.bfloat16, 4, False),
+    (1, 1, 77, 13, 128, torch.bfloat16, 13, True),       # one key per chunk
+    (1, 2, 256, 256, 64, torch.float32, 4, False),       # the tiny workload's layout
+    (1, 1, 130, 390, 64, torch.float32, 2, False),
+    (1, 2, 64, 1024, 128, torch.bfloat16, 1, False),
+]
+
+
+@pytest.mark.parametrize("case", RING_CASES, ids=lambda c: "x".join(map(str, c[:5])) + f"R{c[6]}{'a' if c[7] else ''}{str(c[5])[-4:]}")
+def test_ring_matches_oracle(case):
+    B, H, Sq, Skv, D, dt, R, anything = case
+    g = torch.Generator("cpu").manual_seed(13)
+    q = torch.randn(B, H, Sq, D, generator=g).to(dt)
+    k = torch.randn(B, H, Skv, D, generator=g).to(dt)
+    v = torch.randn(B, H, Skv, D, generator=g).to(dt)
+    out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=R, ring_anything=anything)
+    torch.cuda.synchronize()
+    status_ok()
+    ro, rl = oracle.ring(q, k, v, D ** -0.5, ring_degree=R, ring_anything=anything)
+    to, tl = TOL[dt]
+    assert out.dtype == dt
+    assert maxabs(out, ro) <= to
+    assert maxabs(lse, rl) <= tl
+
+
+def test_ring_large_scores_exercise_rescale():
+    """Scores with std ~12 make the running max grow by more than 2^8
+    between key tiles, so the in-TMEM output rescale runs."""
+    g = torch.Generator("cpu").manual_seed(17)
+    q = (torch.randn(1, 2, 256, 128, generator=g) * 12).to(torch.bfloat16)
+    k = torch.randn(1, 2, 1024, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 2, 1024, 128, generator=g).to(torch.bfloat16)
+    out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=2)
+    torch.cuda.synchronize()
+    ro, rl = oracle.ring(q, k, v, 128 ** -0.5, ring_degree=2)
+    assert maxabs(out, ro) <= 1e-2
+    assert maxabs(lse, rl) <= 1e-3 * max(1.0, float(np.abs(rl).max()) / 8)
+
+
+def test_ring_closed_forms():
+    g = torch.Generator("cpu").manual_seed(19)
+    k = torch.randn(1, 2, 300, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 2, 300, 128, generator=g).to(torch.bfloat16)
+    q0 = torch.zeros(1, 2, 40, 128, dtype=torch.bfloat16)
+    out, lse = cp.ring(q0.to(DEV), k.to(DEV), v.to(DEV), ring_degree=3)
+    torch.cuda.synchronize()
+    mean_v = v.double().mean(dim=2, keepdim=True).expand(1, 2, 40, 128).numpy()
+    assert maxabs(out, mean_v) <= 1e-2
+    assert maxabs(lse, np.full((1, 2, 40), math.log(300))) <= 1e-3
+    c = torch.randn(1, 1, 1, 128, generator=g).to(torch.bfloat16).expand(1, 2, 300, 128).contiguous()
+    q = torch.randn(1, 2, 40, 128, generator=g).to(torch.bfloat16)
+    out, _ = cp.ring(q.to(DEV), k.to(DEV), c.to(DEV), ring_degree=2)
+    torch.cuda.synchronize()
+    assert maxabs(out, c[:, :, :40].double().numpy()) <= 1e-2
+
+
+def test_ring_strided_bshd_inputs_equal_contiguous():
+    g = torch.Generator("cpu").manual_seed(23)
+    x = [torch.randn(1, 300, 4, 128, generator=g).to(torch.bfloat16).to(DEV) for _ in range(3)]
+    views = [t.permute(0, 2, 1, 3) for t in x]           # [B, H, S, D] with stride H*D per token
+    dense = [t.contiguous() for t in views]
+    o1, l1 = cp.ring(*views, ring_degree=2)
+    o2, l2 = cp.ring(*dense, ring_degree=2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_ring_empty_query_is_noop():
+    k = torch.randn(1, 2, 64, 128, device=DEV).to(torch.bfloat16)
+    q = torch.empty(1, 2, 0, 128, device=DEV, dtype=torch.bfloat16)
+    out, lse = cp.ring(q, k, k, ring_degree=2)
+    torch.cuda.synchronize()
+    assert out.shape == (1, 2, 0, 128) and lse.shape == (1, 2, 0)
+
+
+def test_ring_is_deterministic():
+    q, k, v = make_qkv((1, 4, 700, 128), torch.bfloat16, seed=29, device=DEV)
+    a = cp.ring(q, k, v, ring_degree=2)
+    b = cp.ring(q, k, v, ring_degree=2)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

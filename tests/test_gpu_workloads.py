@@ -1,0 +1,106 @@
+"""The five workloads at full size, called exactly as bench.py calls them.
+
+The oracle recomputes sampled query rows one by one (first and last rows,
+tile and chunk boundaries, the ragged tail, random rows, several heads and
+batches); every output row is also checked against properties that hold at
+any size: finite values, and each output coordinate inside the [min, max]
+of the V column it averages (a softmax-weighted mean).
+"""
+import numpy as np
+import pytest
+import torch
+
+import context_attention_partial_gb300 as cp
+import oracle
+from context_attention_partial_gb300.workloads import WORKLOADS, make_workload
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def sample_rows(s, extra_seed=0, n_random=24):
+    rows = {0, 1, 127, 128, 129, 255, 256, s // 2, s - 129, s - 128, s - 2, s - 1}
+    rng = np.random.default_rng(1000 + extra_seed)
+    rows |= set(int(r) for r in rng.integers(0, s, size=n_random))
+    return sorted(r for r in rows if 0 <= r < s)
+
+
+def check_convex(out, v, dims):
+    """out[..., d] lies within [min_j v[j, d], max_j v[j, d]] (+ bf16 slack)."""
+    vmin = v.float().amin(dim=dims, keepdim=True)
+    vmax = v.float().amax(dim=dims, keepdim=True)
+    o = out.float()
+    slack = 1e-2
+    assert torch.isfinite(o).all()
+    assert bool((o >= vmin - slack).all()) and bool((o <= vmax + slack).all())
+
+
+def run_ring_workload(name, heads_to_check):
+    w, q, k, v = make_workload(name, seed=0)
+    gq, gk, gv = q.to(DEV), k.to(DEV), v.to(DEV)
+    out, lse = cp.ring(gq, gk, gv, ring_degree=w.ring_degree, ring_anything=w.ring_anything)
+    torch.cuda.synchronize()
+    assert cp.last_device_status() == 0
+    assert out.dtype == q.dtype and lse.dtype == torch.float32
+    assert torch.isfinite(lse).all()
+    check_convex(out, gv, dims=2)
+    tol_o, tol_l = (2e-3, 1e-3) if w.dtype == "f32" else (1e-2, 1e-3)
+    out_c, lse_c = out.cpu(), lse.cpu()
+    for i, (b, h) in enumerate(heads_to_check):
+        rows = sample_rows(w.seq, i)
+        ro, rl = oracle.ring(q[b, h, rows].unsqueeze(0), k[b, h].unsqueeze(0), v[b, h].unsqueeze(0),
+                             w.head_dim ** -0.5, ring_degree=w.ring_degree,
+                             ring_anything=w.ring_anything)
+        go = out_c[b, h, rows].float().numpy()
+        gl = lse_c[b, h, rows].numpy()
+        assert np.abs(go - ro[0]).max() <= tol_o, (name, b, h)
+        assert np.abs(gl - rl[0]).max() <= tol_l, (name, b, h)
+
+
+def test_tiny_ring_full():
+    w, q, k, v = make_workload("tiny_ring", seed=0)
+    out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=w.ring_degree)
+    torch.cuda.synchronize()
+    ro, rl = oracle.ring(q, k, v, w.head_dim ** -0.5, ring_degree=w.ring_degree)
+    assert out.dtype == torch.float32
+    assert np.abs(out.cpu().numpy() - ro).max() <= 2e-3
+    assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-3
+
+
+def test_flux_ring_sampled():
+    run_ring_workload("flux_ring", [(0, 0), (0, 11), (0, 23)])
+
+
+def test_uneven_ring_sampled():
+    run_ring_workload("uneven_ring", [(0, 0), (1, 7), (1, 23)])
+
+
+@pytest.mark.slow
+def test_video_ring_sampled():
+    run_ring_workload("video_ring", [(0, 0), (0, 17)])
+
+
+def test_ulysses_sampled():
+    w, q, k, v = make_workload("ulysses", seed=0)          # [B, S, H, D]
+    gq, gk, gv = q.to(DEV), k.to(DEV), v.to(DEV)
+    out, lse = cp.ulysses_attention(gq, gk, gv, w.ulysses_degree)
+    torch.cuda.synchronize()
+    assert cp.last_device_status() == 0
+    assert out.shape == q.shape and out.dtype == q.dtype
+    check_convex(out, gv, dims=1)
+    out_c = out.cpu()
+    lse_c = lse.cpu()                                         # [G*B, H/G, S]
+    hg = w.heads // w.ulysses_degree
+    for i, h in enumerate([0, 5, 6, 13, 23]):
+        rows = sample_rows(w.seq, i, n_random=12)
+        qs = q[0, rows, h].unsqueeze(0)
+        ro, rl = oracle.attention(qs, k[0, :, h].unsqueeze(0), v[0, :, h].unsqueeze(0),
+                                  w.head_dim ** -0.5)
+        assert np.abs(out_c[0, rows, h].float().numpy() - ro[0]).max() <= 1e-2
+        assert np.abs(lse_c[h // hg, h % hg, rows].numpy() - rl[0]).max() <= 1e-3
+
+
+def test_workload_table_flops():
+    assert abs(WORKLOADS["flux_ring"].flops / 1e9 - 260.92) < 0.01
+    assert abs(WORKLOADS["uneven_ring"].flops / 1e9 - 522.07) < 0.01
+    assert abs(WORKLOADS["video_ring"].flops / 1e9 - 13194.1) < 0.1
