@@ -12,18 +12,22 @@
 //     lse = max + log1p(exp(min - max)),  o = e^(lse_r - lse) o_r + e^(lse_c - lse) o_c.
 //   With ring_degree = 1 it is a single partial (cpattn_partial).
 //
-// How (one CTA = two 128-row query tiles of one (batch, head)):
+// How (one CTA = two 128-row query tiles of one (batch, head); 12 warps):
 //   warp 8      TMA producer: Q once, then K_j, V_j tiles (128 keys) through a
 //               STAGES-deep shared-memory ring (128-byte swizzle).
 //   warp 9      MMA issuer (one thread): S_i = Q_i K_j^T into TMEM, then
 //               O_i += P_i V_j with P_i read from TMEM (tcgen05.mma, fp32
 //               accumulation), ping-ponging the two query tiles so the tensor
 //               core works on one tile while the other tile's softmax runs.
+//   warp 10     fp32 inputs only: transposes each V tile into a K-major copy
+//               (the tf32 MMA kind takes no MN-major B operand).
 //   warps 0-7   softmax, one warpgroup per query tile, one thread per query
 //               row: S row from TMEM -> row max -> 2^(s*scale*log2e - m)
 //               -> row sum, P (bf16, or fp32 for tf32) back into S's columns;
 //               at each chunk end the normalised partial is merged in fp32
 //               with the running result (held in a global fp32 workspace).
+//   setmaxnreg moves registers from the control warpgroup (warps 8-11) to
+//   the two softmax warpgroups.
 //   TMEM (512 columns): S_0 | S_1 | O_0 | O_1.
 //   The running max is only raised when it grows by more than 2^8 (exponent
 //   8 in log2 units); between raises P values stay below 256, exact enough
@@ -48,13 +52,20 @@ namespace {
 constexpr int kBM = 128;          // query rows per tile (TMEM lanes)
 constexpr int kNT = 2;            // query tiles per CTA
 constexpr int kBN = 128;          // keys per K/V tile
-constexpr int kThreads = 320;     // 8 softmax warps + producer + MMA
-constexpr int kWarpProducer = 8;
+constexpr int kThreads = 384;     // 3 warpgroups
+constexpr int kWarpProducer = 8;  // warpgroup 2: producer, MMA, V transposer, spare
 constexpr int kWarpMma = 9;
+constexpr int kWarpTranspose = 10;
+constexpr int kLaunchRegs = 168;  // registers per thread at launch (65536 / 384, rounded down to 8)
+constexpr int kSoftmaxRegs = 208; // after setmaxnreg: 8 x 32 x 208 + 4 x 32 x 88 = 384 x 168
+constexpr int kControlRegs = 88;
+static_assert(2 * 4 * 32 * kSoftmaxRegs + 4 * 32 * kControlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLn2 = 0.693147180559945309f;
-constexpr unsigned kErrWaitProducer = 1u, kErrWaitMma = 2u, kErrWaitSoftmax = 4u;
+constexpr unsigned kErrWaitProducer = 1u, kErrWaitMma = 2u, kErrWaitSoftmax = 4u,
+                   kErrWaitTranspose = 8u;
 
 template <typename T, int D>
 struct Cfg {
@@ -65,19 +76,24 @@ struct Cfg {
   static constexpr int BOX_COLS = 128 / ES;         // elements per column block
   static constexpr int Q_TILE_BYTES = kBM * ROW_BYTES;
   static constexpr int KV_TILE_BYTES = kBN * ROW_BYTES;
+  // tf32 cannot read an MN-major B operand, so fp32 V tiles are transposed
+  // into K-major copies (rows = D, 128-byte blocks of 32 keys), double-buffered.
+  static constexpr int VT_BUFS = TF32 ? 2 : 0;
+  static constexpr int VT_TILE_BYTES = D * kBN * ES;
   static constexpr int SMEM_BUDGET = 220 * 1024;
-  static constexpr int STAGES_FIT = (SMEM_BUDGET - kNT * Q_TILE_BYTES) / KV_TILE_BYTES;
+  static constexpr int STAGES_FIT =
+      (SMEM_BUDGET - kNT * Q_TILE_BYTES - VT_BUFS * VT_TILE_BYTES) / KV_TILE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int NUM_BARS = 1 + 2 * STAGES + 3 * kNT + 1;
-  static constexpr int SMEM_BYTES =
-      1024 + kNT * Q_TILE_BYTES + STAGES * KV_TILE_BYTES + NUM_BARS * 8 + 16;
+  static constexpr int NUM_BARS = 1 + 2 * STAGES + 3 * kNT + 1 + 2 * VT_BUFS;
+  static constexpr int SMEM_BYTES = 1024 + kNT * Q_TILE_BYTES + STAGES * KV_TILE_BYTES +
+                                    VT_BUFS * VT_TILE_BYTES + NUM_BARS * 8 + 16;
   static constexpr int KSTEP = 32 / ES;             // K elements per MMA (32 bytes)
   static constexpr int QK_STEPS = ROW_BYTES / 32;
   static constexpr int PV_STEPS = kBN / KSTEP;
   static constexpr int P_COLS_PER_STEP = KSTEP * ES / 4;
   static constexpr uint32_t FMT = TF32 ? 2u : 1u;   // tf32 : bf16
   static constexpr uint32_t IDESC_QK = make_idesc(FMT, false, kBM, kBN);
-  static constexpr uint32_t IDESC_PV = make_idesc(FMT, true, kBM, D);
+  static constexpr uint32_t IDESC_PV = make_idesc(FMT, !TF32, kBM, D);
   static constexpr int O_COL = kNT * kBN;
   static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte blocks");
   static_assert(O_COL + kNT * D <= (int)kTmemCols, "TMEM budget");
@@ -94,6 +110,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Byte offset of (row r, byte b of the row) in a tile stored as 128-byte
+// column blocks of `rows` rows each, with the 128-byte swizzle (16-byte
+// chunk index XOR row % 8), the layout TMA writes and tcgen05 reads.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int b, int rows) {
+  return (b >> 7) * rows * 128 + r * 128 + ((((b >> 4) & 7) ^ (r & 7)) << 4) + (b & 15);
+}
 
 // Walks the (chunk, tile) sequence shared by all roles.
 struct TileWalk {
@@ -210,8 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t sQ = smem_addr(smem);
   const uint32_t sKV = sQ + kNT * C::Q_TILE_BYTES;
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + kNT * C::Q_TILE_BYTES + C::STAGES * C::KV_TILE_BYTES);
+  const uint32_t sVt = sKV + C::STAGES * C::KV_TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kNT * C::Q_TILE_BYTES +
+                                               C::STAGES * C::KV_TILE_BYTES +
+                                               C::VT_BUFS * C::VT_TILE_BYTES);
   const uint32_t bar0 = smem_addr(bars);
   const uint32_t BAR_Q = bar0;
   auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
@@ -220,6 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_p = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + kNT + i); };
   auto bar_o = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + 2 * kNT + i); };
   const uint32_t BAR_DRAIN = bar0 + 8u * (1 + 2 * C::STAGES + 3 * kNT);
+  auto bar_vt_full = [&](int i) { return bar0 + 8u * (2 + 2 * C::STAGES + 3 * kNT + i); };
+  auto bar_vt_empty = [&](int i) {
+    return bar0 + 8u * (2 + 2 * C::STAGES + 3 * kNT + C::VT_BUFS + i);
+  };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -239,6 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_o(i), 1);
     }
     mbar_init(BAR_DRAIN, 1);
+    for (int i = 0; i < C::VT_BUFS; ++i) {
+      mbar_init(bar_vt_full(i), 1);
+      mbar_init(bar_vt_empty(i), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -257,126 +290,183 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int c = 0; c < p.ring_degree; ++c)
     n_tiles += ceil_div(p.chunk_start[c + 1] - p.chunk_start[c], kBN);
 
-  if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(BAR_Q, kNT * C::Q_TILE_BYTES);
-      for (int i = 0; i < kNT; ++i)
-        for (int kb = 0; kb < C::NKB; ++kb)
-          tma_load_4d(sQ + i * C::Q_TILE_BYTES + kb * kBM * 128, &tm_q, BAR_Q, kb * C::BOX_COLS,
-                      q_row0 + i * kBM, h, b);
-      int ld = 0;
-      bool ok = true;
-      TileWalk w;
-      w.start(p);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int key0 = p.chunk_start[w.c] + w.t * kBN;
-        for (int which = 0; which < 2; ++which) {
-          const int s = ld % C::STAGES;
-          const uint32_t ph = (ld / C::STAGES) & 1;
-          ok = mbar_wait(bar_empty(s), ph ^ 1, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitProducer);
-          if (!ok) break;
-          mbar_arrive_expect_tx(bar_full(s), C::KV_TILE_BYTES);
-          const CUtensorMap* tm = which == 0 ? &tm_k : &tm_v;
+  if (warp >= 8) {
+    regs_decrease<kControlRegs>();
+    if (warp == kWarpProducer) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        mbar_arrive_expect_tx(BAR_Q, kNT * C::Q_TILE_BYTES);
+        for (int i = 0; i < kNT; ++i)
           for (int kb = 0; kb < C::NKB; ++kb)
-            tma_load_4d(sKV + s * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar_full(s),
-                        kb * C::BOX_COLS, key0, h, b);
-          ++ld;
+            tma_load_4d(sQ + i * C::Q_TILE_BYTES + kb * kBM * 128, &tm_q, BAR_Q,
+                        kb * C::BOX_COLS, q_row0 + i * kBM, h, b);
+        int ld = 0;
+        bool ok = true;
+        TileWalk w;
+        w.start(p);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int key0 = p.chunk_start[w.c] + w.t * kBN;
+          for (int which = 0; which < 2; ++which) {
+            const int s = ld % C::STAGES;
+            const uint32_t ph = (ld / C::STAGES) & 1;
+            ok = mbar_wait(bar_empty(s), ph ^ 1, abort_flag, p.timeout_ns,
+                           &g_cpattn_device_error, kErrWaitProducer);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar_full(s), C::KV_TILE_BYTES);
+            const CUtensorMap* tm = which == 0 ? &tm_k : &tm_v;
+            for (int kb = 0; kb < C::NKB; ++kb)
+              tma_load_4d(sKV + s * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar_full(s),
+                          kb * C::BOX_COLS, key0, h, b);
+            ++ld;
+          }
+          w.next(p);
         }
-        w.next(p);
+        if (!ok) {
+          // leave no copy in flight into this CTA's shared memory
+          mbar_drain(BAR_Q, 0, p.timeout_ns);
+          for (int x = ld > C::STAGES ? ld - C::STAGES : 0; x < ld; ++x)
+            mbar_drain(bar_full(x % C::STAGES), (x / C::STAGES) & 1, p.timeout_ns);
+        }
       }
-      if (!ok) {
-        // leave no copy in flight into this CTA's shared memory
-        mbar_drain(BAR_Q, 0, p.timeout_ns);
-        for (int x = ld > C::STAGES ? ld - C::STAGES : 0; x < ld; ++x)
-          mbar_drain(bar_full(x % C::STAGES), (x / C::STAGES) & 1, p.timeout_ns);
-      }
-    }
-    __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      auto issue_qk = [&](int i, int stage) {
-        const uint32_t d_tmem = tmem + i * kBN;
-        const uint32_t a_base = sQ + i * C::Q_TILE_BYTES;
-        const uint32_t b_base = sKV + stage * C::KV_TILE_BYTES;
+      __syncwarp();
+    } else if (warp == kWarpMma) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        auto issue_qk = [&](int i, int stage) {
+          const uint32_t d_tmem = tmem + i * kBN;
+          const uint32_t a_base = sQ + i * C::Q_TILE_BYTES;
+          const uint32_t b_base = sKV + stage * C::KV_TILE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-          const uint32_t off_a = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
-          const uint32_t off_b = (kk / 4) * (kBN * 128) + (kk % 4) * 32;
-          mma_ss<C::TF32>(d_tmem, smem_desc_sw128(a_base + off_a, 16, 1024),
-                          smem_desc_sw128(b_base + off_b, 16, 1024), C::IDESC_QK, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int i, int stage, uint32_t acc) {
-        const uint32_t d_tmem = tmem + C::O_COL + i * D;
-        const uint32_t a_tmem = tmem + i * kBN;
-        const uint32_t b_base = sKV + stage * C::KV_TILE_BYTES;
+          for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+            const uint32_t off_a = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
+            const uint32_t off_b = (kk / 4) * (kBN * 128) + (kk % 4) * 32;
+            mma_ss<C::TF32>(d_tmem, smem_desc_sw128(a_base + off_a, 16, 1024),
+                            smem_desc_sw128(b_base + off_b, 16, 1024), C::IDESC_QK, kk > 0);
+          }
+        };
+        // P (TMEM) x V: bf16 reads V as an MN-major operand straight from
+        // the TMA tile; tf32 reads the transposed, K-major copy.
+        auto issue_pv = [&](int i, uint32_t v_base, uint32_t acc) {
+          const uint32_t d_tmem = tmem + C::O_COL + i * D;
+          const uint32_t a_tmem = tmem + i * kBN;
 #pragma unroll
-        for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-          mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_STEP,
-                          smem_desc_sw128(b_base + kk * C::KSTEP * 128, kBN * 128, 1024),
-                          C::IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
+          for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+            uint64_t bdesc;
+            if constexpr (C::TF32)
+              bdesc = smem_desc_sw128(v_base + (kk / 4) * (D * 128) + (kk % 4) * 32, 16, 1024);
+            else
+              bdesc = smem_desc_sw128(v_base + kk * C::KSTEP * 128, kBN * 128, 1024);
+            mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_STEP, bdesc, C::IDESC_PV,
+                            (kk > 0 || acc) ? 1u : 0u);
+          }
+        };
+        bool ok = mbar_wait(BAR_Q, 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                            kErrWaitMma);
+        if (ok)
+          ok = mbar_wait(bar_full(0), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                         kErrWaitMma);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(0, 0);
+          mma_commit(bar_s(0));
+          issue_qk(1, 0);
+          mma_commit(bar_s(1));
+          mma_commit(bar_empty(0));
         }
-      };
-      bool ok = mbar_wait(BAR_Q, 0, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
-      if (ok) ok = mbar_wait(bar_full(0), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0, 0);
-        mma_commit(bar_s(0));
-        issue_qk(1, 0);
-        mma_commit(bar_s(1));
-        mma_commit(bar_empty(0));
-      }
-      TileWalk w;
-      w.start(p);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const uint32_t acc = w.t != 0 ? 1u : 0u;
-        const int lv = 2 * j + 1, sv = lv % C::STAGES;
-        const uint32_t phv = (lv / C::STAGES) & 1;
-        const int lk = 2 * j + 2, sk = lk % C::STAGES;
-        const uint32_t phk = (lk / C::STAGES) & 1;
-        const bool more = j + 1 < n_tiles;
-        // query tile 0
-        ok = mbar_wait(bar_p(0), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
-        if (ok) ok = mbar_wait(bar_full(sv), phv, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(0, sv, acc);
-        if (more) {
-          ok = mbar_wait(bar_full(sk), phk, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
+        TileWalk w;
+        w.start(p);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const uint32_t acc = w.t != 0 ? 1u : 0u;
+          const int lv = 2 * j + 1, sv = lv % C::STAGES;
+          const uint32_t phv = (lv / C::STAGES) & 1;
+          const int lk = 2 * j + 2, sk = lk % C::STAGES;
+          const uint32_t phk = (lk / C::STAGES) & 1;
+          const bool more = j + 1 < n_tiles;
+          uint32_t v_base;
+          // query tile 0
+          ok = mbar_wait(bar_p(0), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                         kErrWaitMma);
+          if (!ok) break;
+          if constexpr (C::TF32) {
+            ok = mbar_wait(bar_vt_full(j & 1), (j >> 1) & 1, abort_flag, p.timeout_ns,
+                           &g_cpattn_device_error, kErrWaitMma);
+            v_base = sVt + (j & 1) * C::VT_TILE_BYTES;
+          } else {
+            ok = mbar_wait(bar_full(sv), phv, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                           kErrWaitMma);
+            v_base = sKV + sv * C::KV_TILE_BYTES;
+          }
           if (!ok) break;
           tc_fence_after();
-          issue_qk(0, sk);
-          mma_commit(bar_s(0));
-        } else {
-          mma_commit(bar_o(0));
+          issue_pv(0, v_base, acc);
+          if (more) {
+            ok = mbar_wait(bar_full(sk), phk, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                           kErrWaitMma);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(0, sk);
+            mma_commit(bar_s(0));
+          } else {
+            mma_commit(bar_o(0));
+          }
+          // query tile 1
+          ok = mbar_wait(bar_p(1), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                         kErrWaitMma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, v_base, acc);
+          if constexpr (C::TF32)
+            mma_commit(bar_vt_empty(j & 1));
+          else
+            mma_commit(bar_empty(sv));
+          if (more) {
+            issue_qk(1, sk);
+            mma_commit(bar_s(1));
+            mma_commit(bar_empty(sk));
+          } else {
+            mma_commit(bar_o(1));
+          }
+          w.next(p);
         }
-        // query tile 1
-        ok = mbar_wait(bar_p(1), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitMma);
+        if (!ok) {
+          // let every MMA already issued finish before TMEM is released
+          mma_commit(BAR_DRAIN);
+          mbar_drain(BAR_DRAIN, 0, p.timeout_ns);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kWarpTranspose && C::TF32) {
+      // ---------------------------------------------------------- V transpose (tf32)
+      // V_j [keys x D] as TMA wrote it -> Vt [D x keys], K-major, swizzled.
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int lv = 2 * j + 1, sv = lv % C::STAGES;
+        ok = mbar_wait(bar_full(sv), (lv / C::STAGES) & 1, abort_flag, p.timeout_ns,
+                       &g_cpattn_device_error, kErrWaitTranspose);
+        if (ok)
+          ok = mbar_wait(bar_vt_empty(j & 1), ((j >> 1) & 1) ^ 1, abort_flag, p.timeout_ns,
+                         &g_cpattn_device_error, kErrWaitTranspose);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        tc_fence_after();
-        issue_pv(1, sv, acc);
-        mma_commit(bar_empty(sv));
-        if (more) {
-          issue_qk(1, sk);
-          mma_commit(bar_s(1));
-          mma_commit(bar_empty(sk));
-        } else {
-          mma_commit(bar_o(1));
+        const uint8_t* src = smem + (sKV - sQ) + sv * C::KV_TILE_BYTES;
+        uint8_t* dst = smem + (sVt - sQ) + (j & 1) * C::VT_TILE_BYTES;
+        for (int e = lane; e < kBN * D; e += 32) {
+          const int key = e % kBN, d = e / kBN;
+          const uint32_t v = *reinterpret_cast<const uint32_t*>(src + sw128_offset(key, d * 4, kBN));
+          *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = v;
         }
-        w.next(p);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar_vt_full(j & 1));
+          mbar_arrive(bar_empty(sv));
+        }
       }
-      if (!ok) {
-        // let every MMA already issued finish before TMEM is released
-        mma_commit(BAR_DRAIN);
-        mbar_drain(BAR_DRAIN, 0, p.timeout_ns);
-      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    regs_increase<kSoftmaxRegs>();
     const int wg = warp / 4;
     const int quarter = warp % 4;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -390,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     TileWalk w;
     w.start(p);
     for (int j = 0; j < n_tiles; ++j) {
-      ok = mbar_wait(bar_s(wg), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitSoftmax);
+      ok = mbar_wait(bar_s(wg), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                     kErrWaitSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -405,14 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kBN; ++i)
           if (i >= valid) s[i] = f2u(-INFINITY);
       }
-      float mx[8];
+      float mx[4] = {u2f(s[0]), u2f(s[1]), u2f(s[2]), u2f(s[3])};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = u2f(s[k]);
-#pragma unroll
-      for (int i = 8; i < kBN; ++i) mx[i % 8] = fmaxf(mx[i % 8], u2f(s[i]));
-      const float row_max =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int i = 4; i < kBN; i += 8) {
+        mx[0] = fmax3(mx[0], u2f(s[i + 0]), u2f(s[i + 1]));
+        mx[1] = fmax3(mx[1], u2f(s[i + 2]), u2f(s[i + 3]));
+        if (i + 4 < kBN) {
+          mx[2] = fmax3(mx[2], u2f(s[i + 4]), u2f(s[i + 5]));
+          mx[3] = fmax3(mx[3], u2f(s[i + 6]), u2f(s[i + 7]));
+        }
+      }
+      const float row_max = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
       const float m_tile = row_max * sl2;
       float factor = 1.f;
       bool need = false;
@@ -429,24 +523,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const float neg_m = -m_used;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (!C::TF32) {
-        uint32_t pk[kBN / 2];
 #pragma unroll
-        for (int i = 0; i < kBN / 2; ++i) {
-          const float e0 = ex2_approx(fmaf(u2f(s[2 * i]), sl2, neg_m));
-          const float e1 = ex2_approx(fmaf(u2f(s[2 * i + 1]), sl2, neg_m));
-          acc[i % 4] += e0 + e1;
-          pk[i] = pack_bf16x2(e0, e1);
+      for (int i = 0; i < kBN / 2; ++i) {
+        float x0, x1;
+        ffma2(x0, x1, u2f(s[2 * i]), u2f(s[2 * i + 1]), sl2, sl2, neg_m, neg_m);
+        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+        const int a = 2 * (i & 1);
+        fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], e0, e1);
+        if constexpr (C::TF32) {
+          s[2 * i] = f2u(e0);
+          s[2 * i + 1] = f2u(e1);
+        } else {
+          s[i] = pack_bf16x2(e0, e1);   // P packed in place: s[i] is already consumed
         }
-        tmem_st_x64(tS, pk);
-      } else {
-#pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          const float e = ex2_approx(fmaf(u2f(s[i]), sl2, neg_m));
-          acc[i % 4] += e;
-          s[i] = f2u(e);
-        }
+      }
+      if constexpr (C::TF32) {
         tmem_st_x128(tS, s);
+      } else {
+        tmem_st_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
       }
       l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
       tmem_wait_st();
@@ -456,7 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       w.next(p);
     }
     if (ok) {
-      ok = mbar_wait(bar_o(wg), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error, kErrWaitSoftmax);
+      ok = mbar_wait(bar_o(wg), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                     kErrWaitSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
@@ -478,8 +573,14 @@ cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
                         const AttnParams& p, cudaStream_t stream) {
   using C = Cfg<T, D>;
   auto kernel = attn_fwd_kernel<T, D>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  // The setmaxnreg split assumes exactly kLaunchRegs registers per thread at
+  // launch; with fewer, the softmax warpgroups' increase could never be
+  // granted.  Refuse to launch such a build.
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const dim3 grid((p.s_q + kNT * kBM - 1) / (kNT * kBM), p.heads, p.batch);
   kernel<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, p);

@@ -183,7 +183,10 @@ def test_ring_matches_oracle(case):
 
 def test_ring_large_scores_exercise_rescale():
     """Scores with std ~12 make the running max grow by more than 2^8
-    between key tiles, so the in-TMEM output rescale runs."""
+    between key tiles, so the in-TMEM output rescale runs.  These inputs are
+    not N(0, 1): the softmax is peaked, outputs reach |v| ~ 4, so the bound is
+    the bf16 half-ulp at [2, 4) (2^-7) plus P's bf16 rounding (2^-9 relative)
+    times max |v| (~4): 2e-2."""
     g = torch.Generator("cpu").manual_seed(17)
     q = (torch.randn(1, 2, 256, 128, generator=g) * 12).to(torch.bfloat16)
     k = torch.randn(1, 2, 1024, 128, generator=g).to(torch.bfloat16)
@@ -191,7 +194,7 @@ def test_ring_large_scores_exercise_rescale():
     out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=2)
     torch.cuda.synchronize()
     ro, rl = oracle.ring(q, k, v, 128 ** -0.5, ring_degree=2)
-    assert maxabs(out, ro) <= 1e-2
+    assert maxabs(out, ro) <= 2e-2
     assert maxabs(lse, rl) <= 1e-3 * max(1.0, float(np.abs(rl).max()) / 8)
 
 
