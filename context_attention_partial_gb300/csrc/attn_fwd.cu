@@ -76,17 +76,22 @@ struct Cfg {
   static constexpr int BOX_COLS = 128 / ES;         // elements per column block
   static constexpr int Q_TILE_BYTES = kBM * ROW_BYTES;
   static constexpr int KV_TILE_BYTES = kBN * ROW_BYTES;
-  // tf32 cannot read an MN-major B operand, so fp32 V tiles are transposed
-  // into K-major copies (rows = D, 128-byte blocks of 32 keys), double-buffered.
+  // fp32 inputs: the tf32 MMA kind takes no MN-major B operand, so V tiles
+  // are transposed into K-major copies (rows = D, 128-byte blocks of 32
+  // keys), double-buffered.  Q K^T runs as three tf32 products,
+  // Q_hi K_hi + Q_hi K_lo + Q_lo K_hi (x = hi + lo, hi = x with its low 13
+  // mantissa bits cleared), which keeps scores to about 2^-20 relative; Q_lo
+  // sits in TMEM, K_lo in one shared-memory tile.
   static constexpr int VT_BUFS = TF32 ? 2 : 0;
   static constexpr int VT_TILE_BYTES = D * kBN * ES;
-  static constexpr int SMEM_BUDGET = 220 * 1024;
+  static constexpr int KLO_BYTES = TF32 ? KV_TILE_BYTES : 0;
+  static constexpr int SMEM_BUDGET = (TF32 ? 226 : 220) * 1024;
   static constexpr int STAGES_FIT =
-      (SMEM_BUDGET - kNT * Q_TILE_BYTES - VT_BUFS * VT_TILE_BYTES) / KV_TILE_BYTES;
+      (SMEM_BUDGET - kNT * Q_TILE_BYTES - VT_BUFS * VT_TILE_BYTES - KLO_BYTES) / KV_TILE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int NUM_BARS = 1 + 2 * STAGES + 3 * kNT + 1 + 2 * VT_BUFS;
+  static constexpr int NUM_BARS = 1 + 2 * STAGES + 3 * kNT + 1 + 2 * VT_BUFS + (TF32 ? 3 : 0);
   static constexpr int SMEM_BYTES = 1024 + kNT * Q_TILE_BYTES + STAGES * KV_TILE_BYTES +
-                                    VT_BUFS * VT_TILE_BYTES + NUM_BARS * 8 + 16;
+                                    VT_BUFS * VT_TILE_BYTES + KLO_BYTES + NUM_BARS * 8 + 16;
   static constexpr int KSTEP = 32 / ES;             // K elements per MMA (32 bytes)
   static constexpr int QK_STEPS = ROW_BYTES / 32;
   static constexpr int PV_STEPS = kBN / KSTEP;
@@ -95,8 +100,11 @@ struct Cfg {
   static constexpr uint32_t IDESC_QK = make_idesc(FMT, false, kBM, kBN);
   static constexpr uint32_t IDESC_PV = make_idesc(FMT, !TF32, kBM, D);
   static constexpr int O_COL = kNT * kBN;
+  static constexpr int QLO_COL = O_COL + kNT * D;   // fp32 inputs: Q_lo of tile i at + i*D
   static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte blocks");
   static_assert(O_COL + kNT * D <= (int)kTmemCols, "TMEM budget");
+  static_assert(!TF32 || (D == 64 && QLO_COL + kNT * D <= (int)kTmemCols), "tf32 TMEM budget");
+  static_assert(!TF32 || STAGES % 2 == 0, "fp32 inputs keep K tiles on even stages");
   static_assert(STAGES >= 2, "need at least two K/V stages");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -234,9 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_addr(smem);
   const uint32_t sKV = sQ + kNT * C::Q_TILE_BYTES;
   const uint32_t sVt = sKV + C::STAGES * C::KV_TILE_BYTES;
+  const uint32_t sKlo = sVt + C::VT_BUFS * C::VT_TILE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kNT * C::Q_TILE_BYTES +
                                                C::STAGES * C::KV_TILE_BYTES +
-                                               C::VT_BUFS * C::VT_TILE_BYTES);
+                                               C::VT_BUFS * C::VT_TILE_BYTES + C::KLO_BYTES);
   const uint32_t bar0 = smem_addr(bars);
   const uint32_t BAR_Q = bar0;
   auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
@@ -249,6 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_vt_empty = [&](int i) {
     return bar0 + 8u * (2 + 2 * C::STAGES + 3 * kNT + C::VT_BUFS + i);
   };
+  const uint32_t BAR_QLO = bar0 + 8u * (2 + 2 * C::STAGES + 3 * kNT + 2 * C::VT_BUFS);
+  const uint32_t BAR_KLO_FULL = BAR_QLO + 8u;
+  const uint32_t BAR_KLO_EMPTY = BAR_QLO + 16u;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -260,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR_Q, 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      // fp32 inputs: a K stage is released by the MMA and by the K_lo pass
+      mbar_init(bar_empty(s), (C::TF32 && s % 2 == 0) ? 2 : 1);
     }
     for (int i = 0; i < kNT; ++i) {
       mbar_init(bar_s(i), 1);
@@ -271,6 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::VT_BUFS; ++i) {
       mbar_init(bar_vt_full(i), 1);
       mbar_init(bar_vt_empty(i), 1);
+    }
+    if (C::TF32) {
+      mbar_init(BAR_QLO, 8);   // one arrival per softmax warp
+      mbar_init(BAR_KLO_FULL, 1);
+      mbar_init(BAR_KLO_EMPTY, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -340,8 +358,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < C::QK_STEPS; ++kk) {
             const uint32_t off_a = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
             const uint32_t off_b = (kk / 4) * (kBN * 128) + (kk % 4) * 32;
-            mma_ss<C::TF32>(d_tmem, smem_desc_sw128(a_base + off_a, 16, 1024),
-                            smem_desc_sw128(b_base + off_b, 16, 1024), C::IDESC_QK, kk > 0);
+            const uint64_t bdesc = smem_desc_sw128(b_base + off_b, 16, 1024);
+            mma_ss<C::TF32>(d_tmem, smem_desc_sw128(a_base + off_a, 16, 1024), bdesc, C::IDESC_QK,
+                            kk > 0);
+            if constexpr (C::TF32) {
+              mma_ss<true>(d_tmem, smem_desc_sw128(a_base + off_a, 16, 1024),
+                           smem_desc_sw128(sKlo + off_b, 16, 1024), C::IDESC_QK, 1u);
+              mma_ts<true>(d_tmem, tmem + C::QLO_COL + i * D + kk * C::P_COLS_PER_STEP, bdesc,
+                           C::IDESC_QK, 1u);
+            }
           }
         };
         // P (TMEM) x V: bf16 reads V as an MN-major operand straight from
@@ -365,6 +390,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok)
           ok = mbar_wait(bar_full(0), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
                          kErrWaitMma);
+        if (C::TF32 && ok)
+          ok = mbar_wait(BAR_QLO, 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                         kErrWaitMma) &&
+               mbar_wait(BAR_KLO_FULL, 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                         kErrWaitMma);
         if (ok) {
           tc_fence_after();
           issue_qk(0, 0);
@@ -372,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_qk(1, 0);
           mma_commit(bar_s(1));
           mma_commit(bar_empty(0));
+          if constexpr (C::TF32) mma_commit(BAR_KLO_EMPTY);
         }
         TileWalk w;
         w.start(p);
@@ -402,6 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (more) {
             ok = mbar_wait(bar_full(sk), phk, abort_flag, p.timeout_ns, &g_cpattn_device_error,
                            kErrWaitMma);
+            if (C::TF32 && ok)
+              ok = mbar_wait(BAR_KLO_FULL, (j + 1) & 1, abort_flag, p.timeout_ns,
+                             &g_cpattn_device_error, kErrWaitMma);
             if (!ok) break;
             tc_fence_after();
             issue_qk(0, sk);
@@ -423,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_qk(1, sk);
             mma_commit(bar_s(1));
             mma_commit(bar_empty(sk));
+            if constexpr (C::TF32) mma_commit(BAR_KLO_EMPTY);
           } else {
             mma_commit(bar_o(1));
           }
@@ -436,10 +471,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else if (warp == kWarpTranspose && C::TF32) {
-      // ---------------------------------------------------------- V transpose (tf32)
-      // V_j [keys x D] as TMA wrote it -> Vt [D x keys], K-major, swizzled.
+      // ---------------------------------------------------------- fp32 operand prep
+      // K_j in place -> K_hi (low 13 mantissa bits cleared), K_lo = K - K_hi
+      // into its own tile (same layout); V_j [keys x D] as TMA wrote it ->
+      // Vt [D x keys] (values cleared to tf32 like K_hi), K-major, swizzled.
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
+        const int lk = 2 * j, sk = lk % C::STAGES;
+        ok = mbar_wait(bar_full(sk), (lk / C::STAGES) & 1, abort_flag, p.timeout_ns,
+                       &g_cpattn_device_error, kErrWaitTranspose);
+        if (ok)
+          ok = mbar_wait(BAR_KLO_EMPTY, (j & 1) ^ 1, abort_flag, p.timeout_ns,
+                         &g_cpattn_device_error, kErrWaitTranspose);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        {
+          uint32_t* kt = reinterpret_cast<uint32_t*>(smem + (sKV - sQ) + sk * C::KV_TILE_BYTES);
+          uint32_t* klo = reinterpret_cast<uint32_t*>(smem + (sKlo - sQ));
+          for (int e = lane; e < C::KV_TILE_BYTES / 4; e += 32) {
+            const uint32_t x = kt[e], hi = x & 0xFFFFE000u;
+            kt[e] = hi;
+            klo[e] = f2u(u2f(x) - u2f(hi));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(BAR_KLO_FULL);
+          mbar_arrive(bar_empty(sk));
+        }
         const int lv = 2 * j + 1, sv = lv % C::STAGES;
         ok = mbar_wait(bar_full(sv), (lv / C::STAGES) & 1, abort_flag, p.timeout_ns,
                        &g_cpattn_device_error, kErrWaitTranspose);
@@ -453,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = lane; e < kBN * D; e += 32) {
           const int key = e % kBN, d = e / kBN;
           const uint32_t v = *reinterpret_cast<const uint32_t*>(src + sw128_offset(key, d * 4, kBN));
-          *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = v;
+          *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = v & 0xFFFFE000u;
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -477,9 +537,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    if constexpr (C::TF32) {
+      // this thread's Q row: Q_hi back in place, Q_lo into TMEM
+      ok = mbar_wait(BAR_Q, 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                     kErrWaitSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        uint8_t* qt = smem + wg * C::Q_TILE_BYTES;
+        const int r = quarter * 32 + lane;
+        uint32_t lo[D];
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+          uint32_t* e = reinterpret_cast<uint32_t*>(qt + sw128_offset(r, d * 4, kBM));
+          const uint32_t x = *e, hi = x & 0xFFFFE000u;
+          *e = hi;
+          lo[d] = f2u(u2f(x) - u2f(hi));
+        }
+        fence_proxy_async_smem();
+        tmem_st_x64(tmem + lane_base + C::QLO_COL + wg * D,
+                    *reinterpret_cast<uint32_t(*)[64]>(&lo[0]));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR_QLO);
+      }
+    }
     TileWalk w;
     w.start(p);
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = 0; j < n_tiles && ok; ++j) {
       ok = mbar_wait(bar_s(wg), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error,
                      kErrWaitSoftmax);
       ok = __all_sync(0xffffffffu, ok);

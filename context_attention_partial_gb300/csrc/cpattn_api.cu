@@ -212,7 +212,7 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.ring_degree = ring_degree;
-  p.out_f32 = out_f32 ? 1 : 0;
+  p.out_f32 = out->dtype == CPATTN_F32 ? 1 : 0;
   p.timeout_ns = g_timeout_ns.load();
   for (int c = 0; c <= ring_degree; ++c) p.chunk_start[c] = chunk_start[c];
   const cudaError_t e =
