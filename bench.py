@@ -143,20 +143,27 @@ def barrier(world: int):
         dist.barrier()
 
 
+def _reduce_device():
+    import torch.distributed as dist
+    return "cpu" if dist.get_backend() == "gloo" else "cuda"
+
+
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time (timing is max over ranks)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], device="cuda")
+    t = torch.tensor([x], device=_reduce_device(), dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
 def sum_over_ranks(x: float, world: int) -> float:
+    """Work of all ranks together (value is the whole-job aggregate)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    t = torch.tensor([x], device=_reduce_device(), dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
 
