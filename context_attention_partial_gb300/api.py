@@ -95,6 +95,32 @@ def ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ring_degree: int = 1
     return out, lse
 
 
+def ring_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ring_degree: int = 1,
+                 ring_anything: bool = False, scale: Optional[float] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """``ring`` without a workspace argument, for callers that cannot
+    allocate device memory: the library's own fixed device array (see
+    ``ring_noalloc_max_workspace_bytes``) holds the running merged result.
+    Pass ``out`` and ``lse`` to avoid any allocation here as well.  Calls
+    that overlap on the GPU share that array and race."""
+    lib = _lib.load()
+    B, H, S, D = q.shape
+    if out is None:
+        out = torch.empty(B, H, S, D, device=q.device, dtype=q.dtype)
+    if lse is None:
+        lse = torch.empty(B, H, S, device=q.device, dtype=torch.float32)
+    dq, dk, dv, do, dl = _desc(q), _desc(k), _desc(v), _desc(out), _desc(lse)
+    check(lib.cpattn_ring_noalloc(dq, dk, dv, _scale(scale), int(ring_degree),
+                                  int(bool(ring_anything)), do, dl, _stream_handle(stream)),
+          "cpattn_ring_noalloc")
+    return out, lse
+
+
+def ring_noalloc_max_workspace_bytes() -> int:
+    return int(_lib.load().cpattn_ring_noalloc_max_workspace_bytes())
+
+
 def ulysses_permute(x: torch.Tensor, degree: int, direction: int,
                     out: Optional[torch.Tensor] = None,
                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
@@ -158,6 +184,7 @@ def set_wait_timeout_ns(ns: int) -> None:
     _lib.load().cpattn_set_wait_timeout_ns(int(ns))
 
 
-__all__ = ["partial", "merge", "ring", "ring_workspace_bytes", "ulysses_permute",
+__all__ = ["partial", "merge", "ring", "ring_workspace_bytes", "ring_noalloc",
+           "ring_noalloc_max_workspace_bytes", "ulysses_permute",
            "ulysses_attention", "grouped_as_bhsd", "last_device_status", "set_wait_timeout_ns",
            "CpattnError"]

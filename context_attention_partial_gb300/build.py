@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libcpattn.so")
-SOURCES = ["attn_fwd.cu", "merge_permute.cu", "cpattn_api.cu"]
+SOURCES = ["attn_fwd.cu", "merge_permute.cu", "cpattn_api.cu", "ring_noalloc.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "tmem_ops.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

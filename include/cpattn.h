@@ -22,8 +22,9 @@
  * - Ownership: the caller allocates every input, output and workspace buffer
  *   and keeps it alive until the stream has finished the call.  The library
  *   allocates no device memory and keeps no state between calls except one
- *   device error word (see cpattn_last_device_status).  Descriptors are only
- *   read during the call.
+ *   device error word (see cpattn_last_device_status) and the fixed
+ *   workspace array of cpattn_ring_noalloc (part of the library's static
+ *   device memory).  Descriptors are only read during the call.
  * - Asynchrony: every call is enqueued on `stream` (a cudaStream_t; NULL is the
  *   legacy default stream).  Argument errors are returned synchronously before
  *   anything is launched; a launch failure returns CPATTN_ERR_CUDA.  A wait
@@ -147,6 +148,30 @@ cpattn_status cpattn_ring(const cpattn_tensor* q, const cpattn_tensor* k,
  */
 cpattn_status cpattn_ulysses_permute(const cpattn_tensor* x, int degree,
                                      int dir, cpattn_tensor* y, void* stream);
+
+/*
+ * cpattn_ring_noalloc -- cpattn_ring for callers that cannot allocate device
+ * memory (a fixed device-memory budget, a memory pool that hands out no extra
+ * buffers, a plugin that only receives its input and output pointers).  The
+ * pages have no counterpart: it is an entry point of this library only.
+ * Same arguments and results as cpattn_ring minus the workspace: the running
+ * merged output and LSE live in a fixed array in the library's own device
+ * memory, cpattn_ring_noalloc_max_workspace_bytes() bytes (64 MiB), which
+ * every GPU that loads the library holds until the process exits.  A call
+ * whose cpattn_ring_workspace_bytes() exceeds that returns
+ * CPATTN_ERR_WORKSPACE (1 x 24 x 4608 x 128 fits; larger problems need
+ * cpattn_ring).  The first call on a device looks the array's address up
+ * (cudaGetSymbolAddress); make it before any stream capture.  All calls share
+ * the array: calls whose kernels overlap on the GPU race on it.  Nothing is
+ * allocated or freed by this call.
+ */
+cpattn_status cpattn_ring_noalloc(const cpattn_tensor* q, const cpattn_tensor* k,
+                                  const cpattn_tensor* v, float scale, int ring_degree,
+                                  int ring_anything, cpattn_tensor* out,
+                                  cpattn_tensor* lse, void* stream);
+
+/* Size of the fixed workspace array of cpattn_ring_noalloc, in bytes. */
+size_t cpattn_ring_noalloc_max_workspace_bytes(void);
 
 /* Human-readable name of a status code (static storage). */
 const char* cpattn_status_string(cpattn_status status);
