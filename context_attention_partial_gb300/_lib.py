@@ -23,6 +23,7 @@ EXPORTS = (
     "cpattn_partial", "cpattn_merge", "cpattn_ring_workspace_bytes", "cpattn_ring",
     "cpattn_ulysses_permute", "cpattn_status_string", "cpattn_last_device_status",
     "cpattn_set_wait_timeout_ns", "cpattn_ring_noalloc", "cpattn_ring_noalloc_max_workspace_bytes",
+    "cpattn_set_fault_injection",
 )
 
 
@@ -75,6 +76,8 @@ def load():
         lib.cpattn_last_device_status.argtypes = [vp]
         lib.cpattn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.cpattn_set_wait_timeout_ns.restype = None
+        lib.cpattn_set_fault_injection.argtypes = [i32]
+        lib.cpattn_set_fault_injection.restype = None
         for name in ("cpattn_partial", "cpattn_merge", "cpattn_ring", "cpattn_ulysses_permute",
                      "cpattn_last_device_status", "cpattn_ring_noalloc"):
             getattr(lib, name).restype = ctypes.c_int

@@ -310,93 +310,105 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= 8) {
     regs_decrease<kControlRegs>();
+    // The producer and MMA warps run their schedules with all 32 lanes, so
+    // every index, phase and descriptor stays warp-uniform; lane 0 alone
+    // issues the TMA copies, the MMAs and the commits (a commit tracks the
+    // MMAs of the thread that issues it).
+    auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned code) {
+      const bool r = mbar_wait(bar, parity, abort_flag, p.timeout_ns, &g_cpattn_device_error, code);
+      return __all_sync(0xffffffffu, r);
+    };
+    const bool leader = lane == 0;
     if (warp == kWarpProducer) {
       // ---------------------------------------------------------- producer
-      if (lane == 0) {
+      if (leader) {
         mbar_arrive_expect_tx(BAR_Q, kNT * C::Q_TILE_BYTES);
         for (int i = 0; i < kNT; ++i)
           for (int kb = 0; kb < C::NKB; ++kb)
             tma_load_4d(sQ + i * C::Q_TILE_BYTES + kb * kBM * 128, &tm_q, BAR_Q,
                         kb * C::BOX_COLS, q_row0 + i * kBM, h, b);
-        int ld = 0;
-        bool ok = true;
-        TileWalk w;
-        w.start(p);
-        for (int j = 0; j < n_tiles && ok; ++j) {
-          const int key0 = p.chunk_start[w.c] + w.t * kBN;
-          for (int which = 0; which < 2; ++which) {
-            const int s = ld % C::STAGES;
-            const uint32_t ph = (ld / C::STAGES) & 1;
-            ok = mbar_wait(bar_empty(s), ph ^ 1, abort_flag, p.timeout_ns,
-                           &g_cpattn_device_error, kErrWaitProducer);
-            if (!ok) break;
+      }
+      __syncwarp();
+      int ld = 0;
+      // fault injection (testing): no K/V copies, so every consumer's
+      // bounded wait runs out and the CTA takes the abort path
+      bool ok = p.fault_skip_kv == 0;
+      TileWalk w;
+      w.start(p);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int key0 = p.chunk_start[w.c] + w.t * kBN;
+        for (int which = 0; which < 2; ++which) {
+          const int s = ld % C::STAGES;
+          const uint32_t ph = (ld / C::STAGES) & 1;
+          ok = wait_all(bar_empty(s), ph ^ 1, kErrWaitProducer);
+          if (!ok) break;
+          if (leader) {
             mbar_arrive_expect_tx(bar_full(s), C::KV_TILE_BYTES);
             const CUtensorMap* tm = which == 0 ? &tm_k : &tm_v;
             for (int kb = 0; kb < C::NKB; ++kb)
               tma_load_4d(sKV + s * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar_full(s),
                           kb * C::BOX_COLS, key0, h, b);
-            ++ld;
           }
-          w.next(p);
+          __syncwarp();
+          ++ld;
         }
-        if (!ok) {
-          // leave no copy in flight into this CTA's shared memory
-          mbar_drain(BAR_Q, 0, p.timeout_ns);
-          for (int x = ld > C::STAGES ? ld - C::STAGES : 0; x < ld; ++x)
-            mbar_drain(bar_full(x % C::STAGES), (x / C::STAGES) & 1, p.timeout_ns);
-        }
+        w.next(p);
+      }
+      if (!ok && leader) {
+        // leave no copy in flight into this CTA's shared memory
+        mbar_drain(BAR_Q, 0, p.timeout_ns);
+        for (int x = ld > C::STAGES ? ld - C::STAGES : 0; x < ld; ++x)
+          mbar_drain(bar_full(x % C::STAGES), (x / C::STAGES) & 1, p.timeout_ns);
       }
       __syncwarp();
     } else if (warp == kWarpMma) {
       // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
-        auto issue_qk = [&](int i, int stage) {
-          const uint32_t d_tmem = tmem + i * kBN;
-          const uint32_t a_base = sQ + i * C::Q_TILE_BYTES;
-          const uint32_t b_base = sKV + stage * C::KV_TILE_BYTES;
+      // Descriptors are built once; each MMA only adds a compile-time
+      // constant (byte offset >> 4) to a base.
+      const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t k_desc = smem_desc_sw128(sKV, 16, 1024);
+      const uint64_t v_desc = smem_desc_sw128(sKV, kBN * 128, 1024);
+      const uint64_t vt_desc = C::TF32 ? smem_desc_sw128(sVt, 16, 1024) : 0;
+      const uint64_t klo_desc = C::TF32 ? smem_desc_sw128(sKlo, 16, 1024) : 0;
+      auto issue_qk = [&](int i, int stage) {
+        const uint32_t d_tmem = tmem + i * kBN;
+        const uint64_t a0 = q_desc + static_cast<uint64_t>((i * C::Q_TILE_BYTES) >> 4);
+        const uint64_t b0 = k_desc + static_cast<uint64_t>((stage * C::KV_TILE_BYTES) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-            const uint32_t off_a = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
-            const uint32_t off_b = (kk / 4) * (kBN * 128) + (kk % 4) * 32;
-            const uint64_t bdesc = smem_desc_sw128(b_base + off_b, 16, 1024);
-            mma_ss<C::TF32>(d_tmem, smem_desc_sw128(a_base + off_a, 16, 1024), bdesc, C::IDESC_QK,
-                            kk > 0);
-            if constexpr (C::TF32) {
-              mma_ss<true>(d_tmem, smem_desc_sw128(a_base + off_a, 16, 1024),
-                           smem_desc_sw128(sKlo + off_b, 16, 1024), C::IDESC_QK, 1u);
-              mma_ts<true>(d_tmem, tmem + C::QLO_COL + i * D + kk * C::P_COLS_PER_STEP, bdesc,
-                           C::IDESC_QK, 1u);
-            }
+        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+          const uint64_t off_a = ((kk / 4) * (kBM * 128) + (kk % 4) * 32) >> 4;
+          const uint64_t off_b = ((kk / 4) * (kBN * 128) + (kk % 4) * 32) >> 4;
+          mma_ss<C::TF32>(d_tmem, a0 + off_a, b0 + off_b, C::IDESC_QK, kk > 0);
+          if constexpr (C::TF32) {
+            mma_ss<true>(d_tmem, a0 + off_a, klo_desc + off_b, C::IDESC_QK, 1u);
+            mma_ts<true>(d_tmem, tmem + C::QLO_COL + i * D + kk * C::P_COLS_PER_STEP, b0 + off_b,
+                         C::IDESC_QK, 1u);
           }
-        };
-        // P (TMEM) x V: bf16 reads V as an MN-major operand straight from
-        // the TMA tile; tf32 reads the transposed, K-major copy.
-        auto issue_pv = [&](int i, uint32_t v_base, uint32_t acc) {
-          const uint32_t d_tmem = tmem + C::O_COL + i * D;
-          const uint32_t a_tmem = tmem + i * kBN;
+        }
+      };
+      // P (TMEM) x V: bf16 reads V as an MN-major operand straight from the
+      // TMA tile; tf32 reads the transposed, K-major copy.
+      auto issue_pv = [&](int i, uint64_t b0, uint32_t acc) {
+        const uint32_t d_tmem = tmem + C::O_COL + i * D;
+        const uint32_t a_tmem = tmem + i * kBN;
 #pragma unroll
-          for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-            uint64_t bdesc;
-            if constexpr (C::TF32)
-              bdesc = smem_desc_sw128(v_base + (kk / 4) * (D * 128) + (kk % 4) * 32, 16, 1024);
-            else
-              bdesc = smem_desc_sw128(v_base + kk * C::KSTEP * 128, kBN * 128, 1024);
-            mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_STEP, bdesc, C::IDESC_PV,
-                            (kk > 0 || acc) ? 1u : 0u);
-          }
-        };
-        bool ok = mbar_wait(BAR_Q, 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
-                            kErrWaitMma);
-        if (ok)
-          ok = mbar_wait(bar_full(0), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
-                         kErrWaitMma);
-        if (C::TF32 && ok)
-          ok = mbar_wait(BAR_QLO, 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
-                         kErrWaitMma) &&
-               mbar_wait(BAR_KLO_FULL, 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
-                         kErrWaitMma);
-        if (ok) {
-          tc_fence_after();
+        for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+          uint64_t off_b;
+          if constexpr (C::TF32)
+            off_b = ((kk / 4) * (D * 128) + (kk % 4) * 32) >> 4;
+          else
+            off_b = (kk * C::KSTEP * 128) >> 4;
+          mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_STEP, b0 + off_b, C::IDESC_PV,
+                          (kk > 0 || acc) ? 1u : 0u);
+        }
+      };
+      bool ok = wait_all(BAR_Q, 0, kErrWaitMma);
+      if (ok) ok = wait_all(bar_full(0), 0, kErrWaitMma);
+      if (C::TF32 && ok) ok = wait_all(BAR_QLO, 0, kErrWaitMma);
+      if (C::TF32 && ok) ok = wait_all(BAR_KLO_FULL, 0, kErrWaitMma);
+      if (ok) {
+        tc_fence_after();
+        if (leader) {
           issue_qk(0, 0);
           mma_commit(bar_s(0));
           issue_qk(1, 0);
@@ -404,50 +416,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(bar_empty(0));
           if constexpr (C::TF32) mma_commit(BAR_KLO_EMPTY);
         }
-        TileWalk w;
-        w.start(p);
-        for (int j = 0; j < n_tiles && ok; ++j) {
-          const uint32_t acc = w.t != 0 ? 1u : 0u;
-          const int lv = 2 * j + 1, sv = lv % C::STAGES;
-          const uint32_t phv = (lv / C::STAGES) & 1;
-          const int lk = 2 * j + 2, sk = lk % C::STAGES;
-          const uint32_t phk = (lk / C::STAGES) & 1;
-          const bool more = j + 1 < n_tiles;
-          uint32_t v_base;
-          // query tile 0
-          ok = mbar_wait(bar_p(0), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error,
-                         kErrWaitMma);
-          if (!ok) break;
-          if constexpr (C::TF32) {
-            ok = mbar_wait(bar_vt_full(j & 1), (j >> 1) & 1, abort_flag, p.timeout_ns,
-                           &g_cpattn_device_error, kErrWaitMma);
-            v_base = sVt + (j & 1) * C::VT_TILE_BYTES;
-          } else {
-            ok = mbar_wait(bar_full(sv), phv, abort_flag, p.timeout_ns, &g_cpattn_device_error,
-                           kErrWaitMma);
-            v_base = sKV + sv * C::KV_TILE_BYTES;
-          }
+        __syncwarp();
+      }
+      TileWalk w;
+      w.start(p);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const uint32_t acc = w.t != 0 ? 1u : 0u;
+        const int lv = 2 * j + 1, sv = lv % C::STAGES;
+        const uint32_t phv = (lv / C::STAGES) & 1;
+        const int lk = 2 * j + 2, sk = lk % C::STAGES;
+        const uint32_t phk = (lk / C::STAGES) & 1;
+        const bool more = j + 1 < n_tiles;
+        uint64_t v_base;
+        // query tile 0
+        ok = wait_all(bar_p(0), j & 1, kErrWaitMma);
+        if (!ok) break;
+        if constexpr (C::TF32) {
+          ok = wait_all(bar_vt_full(j & 1), (j >> 1) & 1, kErrWaitMma);
+          v_base = vt_desc + static_cast<uint64_t>(((j & 1) * C::VT_TILE_BYTES) >> 4);
+        } else {
+          ok = wait_all(bar_full(sv), phv, kErrWaitMma);
+          v_base = v_desc + static_cast<uint64_t>((sv * C::KV_TILE_BYTES) >> 4);
+        }
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) issue_pv(0, v_base, acc);
+        __syncwarp();
+        if (more) {
+          ok = wait_all(bar_full(sk), phk, kErrWaitMma);
+          if (C::TF32 && ok) ok = wait_all(BAR_KLO_FULL, (j + 1) & 1, kErrWaitMma);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(0, v_base, acc);
-          if (more) {
-            ok = mbar_wait(bar_full(sk), phk, abort_flag, p.timeout_ns, &g_cpattn_device_error,
-                           kErrWaitMma);
-            if (C::TF32 && ok)
-              ok = mbar_wait(BAR_KLO_FULL, (j + 1) & 1, abort_flag, p.timeout_ns,
-                             &g_cpattn_device_error, kErrWaitMma);
-            if (!ok) break;
-            tc_fence_after();
+          if (leader) {
             issue_qk(0, sk);
             mma_commit(bar_s(0));
-          } else {
-            mma_commit(bar_o(0));
           }
-          // query tile 1
-          ok = mbar_wait(bar_p(1), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error,
-                         kErrWaitMma);
-          if (!ok) break;
-          tc_fence_after();
+        } else if (leader) {
+          mma_commit(bar_o(0));
+        }
+        __syncwarp();
+        // query tile 1
+        ok = wait_all(bar_p(1), j & 1, kErrWaitMma);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
           issue_pv(1, v_base, acc);
           if constexpr (C::TF32)
             mma_commit(bar_vt_empty(j & 1));
@@ -461,13 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             mma_commit(bar_o(1));
           }
-          w.next(p);
         }
-        if (!ok) {
-          // let every MMA already issued finish before TMEM is released
-          mma_commit(BAR_DRAIN);
-          mbar_drain(BAR_DRAIN, 0, p.timeout_ns);
-        }
+        __syncwarp();
+        w.next(p);
+      }
+      if (!ok && leader) {
+        // let every MMA already issued finish before TMEM is released
+        mma_commit(BAR_DRAIN);
+        mbar_drain(BAR_DRAIN, 0, p.timeout_ns);
       }
       __syncwarp();
     } else if (warp == kWarpTranspose && C::TF32) {

@@ -23,6 +23,7 @@ namespace {
 using cpattn::InDtype;
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_fault_skip_kv{0};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -214,6 +215,7 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   p.ring_degree = ring_degree;
   p.out_f32 = out->dtype == CPATTN_F32 ? 1 : 0;
   p.timeout_ns = g_timeout_ns.load();
+  p.fault_skip_kv = g_fault_skip_kv.load();
   for (int c = 0; c <= ring_degree; ++c) p.chunk_start[c] = chunk_start[c];
   const cudaError_t e =
       cpattn::launch_attention(q->dtype == CPATTN_BF16 ? InDtype::BF16 : InDtype::F32,
@@ -353,5 +355,7 @@ cpattn_status cpattn_last_device_status(void* stream) {
 }
 
 void cpattn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+void cpattn_set_fault_injection(int mode) { g_fault_skip_kv.store(mode == 1 ? 1 : 0); }
 
 }  // extern "C"

@@ -190,6 +190,16 @@ cpattn_status cpattn_last_device_status(void* stream);
  */
 void cpattn_set_wait_timeout_ns(uint64_t ns);
 
+/*
+ * cpattn_set_fault_injection -- testing hook for the failure path.  mode 1:
+ * the TMA producer of every following attention launch issues no K/V
+ * copies, so the consumers' bounded waits run out; each CTA then drains what
+ * it has in flight, frees its TMEM and returns, and cpattn_last_device_status
+ * reports CPATTN_ERR_TIMEOUT (outputs are not written).  mode 0 (default):
+ * normal operation.  Process-wide, read at each launch.
+ */
+void cpattn_set_fault_injection(int mode);
+
 #ifdef __cplusplus
 }
 #endif
