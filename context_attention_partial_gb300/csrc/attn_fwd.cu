@@ -428,7 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t phk = (lk / C::STAGES) & 1;
         const bool more = j + 1 < n_tiles;
         uint64_t v_base;
-        // query tile 0
+        // query tile 0: every wait of the group (P_0, V_j, K_{j+1}) comes
+        // before the first MMA, so the 16 MMAs go out back to back: the
+        // hardware MMA queue is only a few MMAs deep and drains during any
+        // wait placed between them.
         ok = wait_all(bar_p(0), j & 1, kErrWaitMma);
         if (!ok) break;
         if constexpr (C::TF32) {
@@ -438,21 +441,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_all(bar_full(sv), phv, kErrWaitMma);
           v_base = v_desc + static_cast<uint64_t>((sv * C::KV_TILE_BYTES) >> 4);
         }
+        if (ok && more) ok = wait_all(bar_full(sk), phk, kErrWaitMma);
+        if (C::TF32 && ok && more) ok = wait_all(BAR_KLO_FULL, (j + 1) & 1, kErrWaitMma);
         if (!ok) break;
         tc_fence_after();
-        if (leader) issue_pv(0, v_base, acc);
-        __syncwarp();
-        if (more) {
-          ok = wait_all(bar_full(sk), phk, kErrWaitMma);
-          if (C::TF32 && ok) ok = wait_all(BAR_KLO_FULL, (j + 1) & 1, kErrWaitMma);
-          if (!ok) break;
-          tc_fence_after();
-          if (leader) {
+        if (leader) {
+          issue_pv(0, v_base, acc);
+          if (more) {
             issue_qk(0, sk);
             mma_commit(bar_s(0));
+          } else {
+            mma_commit(bar_o(0));
           }
-        } else if (leader) {
-          mma_commit(bar_o(0));
         }
         __syncwarp();
         // query tile 1
