@@ -200,15 +200,17 @@ def ring_workload_step(name, dev):
     return w, step, (q, k, v, out, lse, ws)
 
 
-def ulysses_step(dev):
+def ulysses_step(dev, name="ulysses"):
+    """Ulysses (ring_degree 1) or Unified (ring_degree > 1) step: three
+    permutes, one attention launch over all head groups, one inverse permute."""
     import context_attention_partial_gb300 as cp
     from context_attention_partial_gb300.workloads import make_workload
-    w, q, k, v = make_workload("ulysses", seed=0)
+    w, q, k, v = make_workload(name, seed=0)
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
     bufs = {}
 
     def step():
-        cp.ulysses_attention(q, k, v, w.ulysses_degree, buffers=bufs)
+        cp.unified_attention(q, k, v, w.ulysses_degree, w.ring_degree, buffers=bufs)
     return w, step, (q, k, v, bufs)
 
 
@@ -251,15 +253,28 @@ def e2e_ring(name, dev, steps, stream):
     return ms, h2d, d2h, w.flops
 
 
-def time_batch(fn, calls: int, flush: torch.Tensor, stream):
-    """One L2 flush, then `calls` back-to-back calls between two CUDA events
-    on `stream`; returns ms per call.  Callers rotate buffer sets whose total
-    exceeds L2, so every call streams from HBM."""
+def time_graph(fn, calls: int, flush: torch.Tensor, stream):
+    """`calls` back-to-back calls captured into one CUDA graph (so host-side
+    argument marshalling does not pace the GPU), replayed after an L2 flush
+    between two CUDA events; returns ms per call.  Callers rotate buffer sets
+    whose total exceeds L2, so every call streams from HBM."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(calls):
+            fn()
+    graph.replay()
+    torch.cuda.synchronize()
     flush.fill_(7)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(calls):
-        fn()
+    graph.replay()
     b.record(stream)
     torch.cuda.synchronize()
     return a.elapsed_time(b) / calls
@@ -288,10 +303,10 @@ def aux_measurements(dev, stream, peaks):
             cp.merge(*a)
         for _ in range(5):
             mstep()
-        ms = time_batch(mstep, 40, flush, stream)
+        ms = time_graph(mstep, 40, flush, stream)
         gbs = nbytes / (ms * 1e-3) / 1e9
         aux[label] = {"ms": ms, "GB/s": gbs, "bytes": nbytes, "frac_hbm": gbs / peaks["hbm_gbs"],
-                      "timing": "40 back-to-back calls over rotating sets > L2"}
+                      "timing": "40 calls in one CUDA graph over rotating sets > L2"}
         del sets
     # permute at the Ulysses workload, 8 rotating sets (453 MB > L2)
     from context_attention_partial_gb300.workloads import make_qkv
@@ -305,12 +320,12 @@ def aux_measurements(dev, stream, peaks):
         cp.ulysses_permute(xs[i], 4, 1, out=ys[i])
     for _ in range(5):
         pstep()
-    ms = time_batch(pstep, 80, flush, stream)
+    ms = time_graph(pstep, 80, flush, stream)
     nbytes = 2 * xs[0].numel() * 2
     gbs = nbytes / (ms * 1e-3) / 1e9
     aux["permute_ulysses"] = {"ms": ms, "GB/s": gbs, "bytes": nbytes,
                               "frac_hbm": gbs / peaks["hbm_gbs"],
-                              "timing": "80 back-to-back calls over 8 rotating sets > L2"}
+                              "timing": "80 calls in one CUDA graph over 8 rotating sets > L2"}
     del xs, ys
     # the other attention workloads
     for name in ("uneven_ring", "video_ring", "tiny_ring"):
@@ -322,14 +337,16 @@ def aux_measurements(dev, stream, peaks):
         aux[name] = {"ms": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12,
                      "frac_bf16_peak": w.flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
         del keep
-    w, step, keep = ulysses_step(dev)
-    for _ in range(3):
-        step()
-    times = time_steps(step, 30, flush, stream)
-    ms = statistics.median(times)
-    aux["ulysses"] = {"ms": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12,
-                      "launches_per_step": 5,
-                      "frac_bf16_peak": w.flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+    for name in ("ulysses", "unified"):
+        w, step, keep = ulysses_step(dev, name)
+        for _ in range(3):
+            step()
+        times = time_steps(step, 30, flush, stream)
+        ms = statistics.median(times)
+        aux[name] = {"ms": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12,
+                     "launches_per_step": 5,
+                     "frac_bf16_peak": w.flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+        del keep
     return aux
 
 

@@ -145,14 +145,21 @@ def grouped_as_bhsd(t: torch.Tensor) -> torch.Tensor:
     return t.view(G * B, S, Hg, D).permute(0, 2, 1, 3)
 
 
-def ulysses_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, degree: int,
-                      scale: Optional[float] = None,
+def unified_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ulysses_degree: int,
+                      ring_degree: int = 1, scale: Optional[float] = None,
                       stream: Optional[torch.cuda.Stream] = None,
                       buffers: Optional[dict] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Ulysses on one GPU: permute q, k, v [B,S,H,D] into G head groups, full
-    attention per group (one launch over all groups), inverse permute of the
-    output.  Returns (out [B,S,H,D], lse f32 [G*B, H/G, S])."""
+    """Unified (Ulysses x Ring) attention on one GPU (Diffusers "Context
+    parallelism", "Unified Attention": an all-to-all regroups heads and
+    tokens, Ring Attention runs on the result, the all-to-all is reversed).
+    q, k, v [B,S,H,D]: permute into G = ulysses_degree head groups, ring
+    attention with ring_degree chunks over each group's full sequence (one
+    launch for all groups), inverse permute of the output.  ring_degree 1 is
+    plain Ulysses.  Returns (out [B,S,H,D], lse f32 [G*B, H/G, S]).
+    `buffers` (a dict) keeps the grouped tensors and the ring workspace
+    between calls."""
     B, S, H, D = q.shape
+    G, R = int(ulysses_degree), int(ring_degree)
     bufs = buffers if buffers is not None else {}
 
     def buf(name, shape, dtype):
@@ -162,16 +169,30 @@ def ulysses_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, degree:
             bufs[name] = t
         return t
 
-    G = degree
-    qg = ulysses_permute(q, G, 1, out=buf("q", (G, B, S, H // G, D), q.dtype), stream=stream)
-    kg = ulysses_permute(k, G, 1, out=buf("k", (G, B, S, H // G, D), k.dtype), stream=stream)
-    vg = ulysses_permute(v, G, 1, out=buf("v", (G, B, S, H // G, D), v.dtype), stream=stream)
-    og = buf("o", (G, B, S, H // G, D), q.dtype)
+    gshape = (G, B, S, H // max(G, 1), D)
+    qg = ulysses_permute(q, G, 1, out=buf("q", gshape, q.dtype), stream=stream)
+    kg = ulysses_permute(k, G, 1, out=buf("k", gshape, k.dtype), stream=stream)
+    vg = ulysses_permute(v, G, 1, out=buf("v", gshape, v.dtype), stream=stream)
+    og = buf("o", gshape, q.dtype)
     lse = buf("lse", (G * B, H // G, S), torch.float32)
-    ring(grouped_as_bhsd(qg), grouped_as_bhsd(kg), grouped_as_bhsd(vg), 1, False, scale,
-         out=grouped_as_bhsd(og), lse=lse, stream=stream)
+    qv = grouped_as_bhsd(qg)
+    need = ring_workspace_bytes(qv, R)
+    ws = buf("ws", (max(need, 16),), torch.uint8) if need > 0 else None
+    ring(qv, grouped_as_bhsd(kg), grouped_as_bhsd(vg), R, False, scale,
+         out=grouped_as_bhsd(og), lse=lse, workspace=ws, stream=stream)
     out = ulysses_permute(og, G, -1, out=buf("out", (B, S, H, D), q.dtype), stream=stream)
     return out, lse
+
+
+def ulysses_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, degree: int,
+                      scale: Optional[float] = None,
+                      stream: Optional[torch.cuda.Stream] = None,
+                      buffers: Optional[dict] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Ulysses on one GPU (Diffusers "Context parallelism", "Ulysses
+    Attention"): permute q, k, v [B,S,H,D] into G head groups, full attention
+    per group (one launch over all groups), inverse permute of the output.
+    Returns (out [B,S,H,D], lse f32 [G*B, H/G, S])."""
+    return unified_attention(q, k, v, degree, 1, scale, stream, buffers)
 
 
 def last_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
@@ -185,6 +206,6 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 
 __all__ = ["partial", "merge", "ring", "ring_workspace_bytes", "ring_noalloc",
-           "ring_noalloc_max_workspace_bytes", "ulysses_permute",
+           "ring_noalloc_max_workspace_bytes", "ulysses_permute", "unified_attention",
            "ulysses_attention", "grouped_as_bhsd", "last_device_status", "set_wait_timeout_ns",
            "CpattnError"]

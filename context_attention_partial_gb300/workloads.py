@@ -66,6 +66,10 @@ WORKLOADS = {
         Workload("uneven_ring", 2, 24, 4609, 128, "bf16", ring_degree=3, ring_anything=True,
                  description="ring_anything uneven split: bf16 [2,24,4609,128], "
                              "ring_degree 3"),
+        Workload("unified", 1, 24, 4608, 128, "bf16", ring_degree=2, ulysses_degree=2,
+                 layout="bshd",
+                 description="Unified (Ulysses x Ring) on the FLUX-like shape: bf16 "
+                             "[1,4608,24,128] (B,S,H,D), ulysses_degree 2, ring_degree 2"),
     ]
 }
 

@@ -23,6 +23,9 @@ Functions and the passages they follow (page title, section):
 * ``ring``        -- partials over every chunk folded with ``merge``.
 * ``ulysses_permute`` -- the head regroup of Diffusers "Context parallelism",
   "Ulysses Attention", as a layout permute.
+* ``unified``     -- Diffusers "Context parallelism", "Unified Attention":
+  regroup, ring within each group, inverse regroup (composition of the
+  functions above).
 """
 from __future__ import annotations
 
@@ -257,6 +260,20 @@ def ulysses_permute(x, degree: int, direction: int):
         yt = torch.from_numpy(y)
         return yt.view(x.dtype) if yt.dtype != x.dtype else yt
     return y
+
+
+def unified(q, k, v, ulysses_degree: int, ring_degree: int = 1, scale=None):
+    """Unified (Ulysses x Ring) attention as the steps of Diffusers "Context
+    parallelism", "Unified Attention": head regroup of q, k, v [B, S, H, D]
+    into G groups (``ulysses_permute``), the ring schedule with ring_degree
+    chunks over each group's full sequence (``ring``), inverse regroup of the
+    output.  Returns (out [B, S, H, D] float64, lse [G, B, H/G, S])."""
+    G, R = int(ulysses_degree), int(ring_degree)
+    qg, kg, vg = (ulysses_permute(_f64(x), G, 1) for x in (q, k, v))   # [G, B, S, Hg, D]
+    to_bhsd = lambda t: np.ascontiguousarray(np.transpose(t, (0, 1, 3, 2, 4)))   # [G, B, Hg, S, D]
+    o, l = ring(to_bhsd(qg), to_bhsd(kg), to_bhsd(vg), scale, ring_degree=R)
+    og = np.ascontiguousarray(np.transpose(o, (0, 1, 3, 2, 4)))        # [G, B, S, Hg, D]
+    return ulysses_permute(og, G, -1), l
 
 
 def num_threads() -> int:

@@ -240,3 +240,23 @@ def test_ring_is_deterministic():
     b = cp.ring(q, k, v, ring_degree=2)
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("b,s,h,d,g,r,dt", [
+    (1, 300, 8, 128, 2, 3, torch.bfloat16),
+    (2, 256, 6, 64, 3, 2, torch.bfloat16),
+    (1, 256, 4, 64, 2, 4, torch.float32),
+    (1, 130, 4, 128, 4, 1, torch.bfloat16),
+])
+def test_unified_matches_oracle(b, s, h, d, g, r, dt):
+    """Unified (Ulysses x Ring): regroup, ring inside each head group,
+    inverse regroup -- against the oracle's composition of the same steps."""
+    q, k, v = make_qkv((b, s, h, d), dt, seed=37)
+    out, lse = cp.unified_attention(q.to(DEV), k.to(DEV), v.to(DEV), g, r)
+    torch.cuda.synchronize()
+    status_ok()
+    ro, rl = oracle.unified(q, k, v, g, r, d ** -0.5)
+    to, tl = TOL[dt]
+    assert out.shape == q.shape and out.dtype == dt
+    assert maxabs(out, ro) <= to
+    assert maxabs(lse.reshape(g, b, h // g, s), rl) <= tl

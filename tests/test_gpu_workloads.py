@@ -100,6 +100,26 @@ def test_ulysses_sampled():
         assert np.abs(lse_c[h // hg, h % hg, rows].numpy() - rl[0]).max() <= 1e-3
 
 
+def test_unified_sampled():
+    """Unified on the FLUX-like shape (ulysses_degree 2, ring_degree 2): each
+    head's rows equal the ring schedule over that head's full sequence."""
+    w, q, k, v = make_workload("unified", seed=0)          # [B, S, H, D]
+    out, lse = cp.unified_attention(q.to(DEV), k.to(DEV), v.to(DEV), w.ulysses_degree,
+                                    w.ring_degree)
+    torch.cuda.synchronize()
+    assert cp.last_device_status() == 0
+    check_convex(out, v.to(DEV), dims=1)
+    out_c, lse_c = out.cpu(), lse.cpu()
+    hg = w.heads // w.ulysses_degree
+    for i, h in enumerate([0, 11, 12, 23]):
+        rows = sample_rows(w.seq, i, n_random=12)
+        ro, rl = oracle.ring(q[0, rows, h].unsqueeze(0), k[0, :, h].unsqueeze(0),
+                             v[0, :, h].unsqueeze(0), w.head_dim ** -0.5,
+                             ring_degree=w.ring_degree)
+        assert np.abs(out_c[0, rows, h].float().numpy() - ro[0]).max() <= 1e-2
+        assert np.abs(lse_c[h // hg, h % hg, rows].numpy() - rl[0]).max() <= 1e-3
+
+
 def test_workload_table_flops():
     assert abs(WORKLOADS["flux_ring"].flops / 1e9 - 260.92) < 0.01
     assert abs(WORKLOADS["uneven_ring"].flops / 1e9 - 522.07) < 0.01

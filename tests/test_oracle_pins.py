@@ -244,6 +244,21 @@ def pin_ulysses_permute():
         oracle.ulysses_permute(np.zeros((1, 2, 6, 4), np.int32), 4, 1)
 
 
+def pin_unified_is_full_attention():
+    """Diffusers "Context parallelism", "Unified Attention": regroup, ring on
+    the result, reverse the regroup -- still every query meets every key of
+    its head once, so the result is full attention per head."""
+    for (b, s, h, d, g, r) in [(1, 12, 4, 3, 2, 3), (2, 8, 6, 4, 3, 2), (1, 10, 4, 2, 4, 5),
+                               (1, 9, 2, 2, 1, 3), (1, 7, 6, 2, 6, 1)]:
+        q, k, v = _rand(b, s, h, d), _rand(b, s, h, d), _rand(b, s, h, d)
+        o, l = oracle.unified(q, k, v, g, r, 0.6)
+        bhsd = lambda t: np.transpose(t, (0, 2, 1, 3))
+        ro, rl = oracle.attention(bhsd(q), bhsd(k), bhsd(v), 0.6)   # [B, H, S, D]
+        assert np.allclose(o, np.transpose(ro, (0, 2, 1, 3)), atol=1e-12)
+        lg = l.reshape(g, b, h // g, s).transpose(1, 0, 2, 3).reshape(b, h, s)
+        assert np.allclose(lg, rl, atol=1e-12)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
