@@ -64,12 +64,13 @@ def build(force: bool = False) -> str:
 def _bind(path: str):
     lib = ctypes.CDLL(path)
     d, i64, p = ctypes.c_double, ctypes.c_int64, ctypes.c_void_p
-    lib.cpo_attention_rows.argtypes = [p, p, p, i64, i64, i64, i64, d, p, i64, p, p]
-    lib.cpo_partial_rows.argtypes = [p, p, p, i64, i64, i64, i64, d, i64, i64, p, i64, p, p]
+    ci = ctypes.c_int
+    lib.cpo_attention_rows.argtypes = [p, p, p, i64, i64, i64, i64, d, p, i64, p, p, ci]
+    lib.cpo_partial_rows.argtypes = [p, p, p, i64, i64, i64, i64, d, i64, i64, p, i64, p, p, ci]
     lib.cpo_merge.argtypes = [p, p, p, p, i64, i64]
     lib.cpo_merge.restype = None
     lib.cpo_chunk_bounds.argtypes = [i64, i64, ctypes.c_int, p]
-    lib.cpo_ring_rows.argtypes = [p, p, p, i64, i64, i64, i64, d, i64, ctypes.c_int, p, i64, p, p]
+    lib.cpo_ring_rows.argtypes = [p, p, p, i64, i64, i64, i64, d, i64, ctypes.c_int, p, i64, p, p, ci]
     lib.cpo_ulysses_permute.argtypes = [p, p, i64, i64, i64, i64, i64, ctypes.c_int, i64]
     lib.cpo_num_threads.argtypes = []
     for name in ("cpo_attention_rows", "cpo_partial_rows", "cpo_chunk_bounds",
@@ -167,21 +168,22 @@ def _shape_out(lead, s_q, d, rows, n, out, lse):
     return out.reshape(n, d), lse.reshape(n)
 
 
-def attention(q, k, v, scale=None, rows=None):
+def attention(q, k, v, scale=None, rows=None, causal=False):
     """Full softmax attention (the definition).  q [..., S_q, D],
     k, v [..., S_kv, D].  ``rows``: optional flat indices into the
-    [prod(...) * S_q] query rows; then out is [n, D] and lse [n]."""
+    [prod(...) * S_q] query rows; then out is [n, D] and lse [n].
+    ``causal``: query i attends keys j <= i (is_causal)."""
     q, k, v, lead, nbh, s_q, s_kv, d = _flatten(q, k, v)
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
     r, n = _rows(rows, nbh, s_q)
     out = np.empty((n, d)); lse = np.empty(n)
     _check(_load().cpo_attention_rows(_ptr(q), _ptr(k), _ptr(v), nbh, s_q, s_kv, d,
                                       scale, None if r is None else _ptr(r), n,
-                                      _ptr(out), _ptr(lse)))
+                                      _ptr(out), _ptr(lse), int(bool(causal))))
     return _shape_out(lead, s_q, d, r, n, out, lse)
 
 
-def partial(q, k, v, scale=None, k0=0, k1=None, rows=None):
+def partial(q, k, v, scale=None, k0=0, k1=None, rows=None, causal=False):
     """One ring step: attention over keys [k0, k1) only -> (out, lse)."""
     q, k, v, lead, nbh, s_q, s_kv, d = _flatten(q, k, v)
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
@@ -190,7 +192,7 @@ def partial(q, k, v, scale=None, k0=0, k1=None, rows=None):
     out = np.empty((n, d)); lse = np.empty(n)
     _check(_load().cpo_partial_rows(_ptr(q), _ptr(k), _ptr(v), nbh, s_q, s_kv, d, scale,
                                     k0, k1, None if r is None else _ptr(r), n,
-                                    _ptr(out), _ptr(lse)))
+                                    _ptr(out), _ptr(lse), int(bool(causal))))
     return _shape_out(lead, s_q, d, r, n, out, lse)
 
 
@@ -212,7 +214,7 @@ def chunk_bounds(s_kv: int, ring_degree: int, ring_anything: bool = False):
     return [int(x) for x in b]
 
 
-def ring(q, k, v, scale=None, ring_degree=1, ring_anything=False, rows=None):
+def ring(q, k, v, scale=None, ring_degree=1, ring_anything=False, rows=None, causal=False):
     """The ring schedule: a partial per chunk, folded with ``merge`` in
     chunk order 0..R-1."""
     q, k, v, lead, nbh, s_q, s_kv, d = _flatten(q, k, v)
@@ -221,7 +223,8 @@ def ring(q, k, v, scale=None, ring_degree=1, ring_anything=False, rows=None):
     out = np.empty((n, d)); lse = np.empty(n)
     _check(_load().cpo_ring_rows(_ptr(q), _ptr(k), _ptr(v), nbh, s_q, s_kv, d, scale,
                                  ring_degree, int(bool(ring_anything)),
-                                 None if r is None else _ptr(r), n, _ptr(out), _ptr(lse)))
+                                 None if r is None else _ptr(r), n, _ptr(out), _ptr(lse),
+                                 int(bool(causal))))
     return _shape_out(lead, s_q, d, r, n, out, lse)
 
 
@@ -262,7 +265,7 @@ def ulysses_permute(x, degree: int, direction: int):
     return y
 
 
-def unified(q, k, v, ulysses_degree: int, ring_degree: int = 1, scale=None):
+def unified(q, k, v, ulysses_degree: int, ring_degree: int = 1, scale=None, causal=False):
     """Unified (Ulysses x Ring) attention as the steps of Diffusers "Context
     parallelism", "Unified Attention": head regroup of q, k, v [B, S, H, D]
     into G groups (``ulysses_permute``), the ring schedule with ring_degree
@@ -271,7 +274,7 @@ def unified(q, k, v, ulysses_degree: int, ring_degree: int = 1, scale=None):
     G, R = int(ulysses_degree), int(ring_degree)
     qg, kg, vg = (ulysses_permute(_f64(x), G, 1) for x in (q, k, v))   # [G, B, S, Hg, D]
     to_bhsd = lambda t: np.ascontiguousarray(np.transpose(t, (0, 1, 3, 2, 4)))   # [G, B, Hg, S, D]
-    o, l = ring(to_bhsd(qg), to_bhsd(kg), to_bhsd(vg), scale, ring_degree=R)
+    o, l = ring(to_bhsd(qg), to_bhsd(kg), to_bhsd(vg), scale, ring_degree=R, causal=causal)
     og = np.ascontiguousarray(np.transpose(o, (0, 1, 3, 2, 4)))        # [G, B, S, Hg, D]
     return ulysses_permute(og, G, -1), l
 

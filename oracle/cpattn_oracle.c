@@ -39,11 +39,13 @@
  *    lse_i = log sum_j exp(scale * q_i . k_j)   (natural log), written as
  *    M + log(sum_j exp(s_j - M)) with M = max_j s_j so exp never overflows.
  *    row_ids: flat indices into [NBH * S_q]; NULL means every row.
+ *    causal != 0: scaled_dot_product_attention's is_causal, i.e. query i
+ *    attends keys j <= i only; a row with no such key gives (0, -inf).
  * ------------------------------------------------------------------------- */
 int cpo_attention_rows(const double* q, const double* k, const double* v,
                        int64_t nbh, int64_t s_q, int64_t s_kv, int64_t d,
                        double scale, const int64_t* row_ids, int64_t n_rows,
-                       double* out, double* lse) {
+                       double* out, double* lse, int causal) {
   if (s_kv < 1) return CPO_ERR_SHAPE;
   if (row_ids == NULL) n_rows = nbh * s_q;
   int failed = 0;
@@ -59,23 +61,31 @@ int cpo_attention_rows(const double* q, const double* k, const double* v,
       if (s == NULL) continue;
       int64_t row = row_ids ? row_ids[r] : r;
       int64_t bh = row / s_q;
+      int64_t i = row % s_q;
       const double* qi = q + row * d;
       const double* kb = k + bh * s_kv * d;
       const double* vb = v + bh * s_kv * d;
+      /* the keys this row attends: all, or j <= i when causal */
+      int64_t n_keys = s_kv;
+      if (causal && i + 1 < s_kv) n_keys = i + 1;
+      double* oi = out + r * d;
+      for (int64_t e = 0; e < d; ++e) oi[e] = 0.0;
+      if (n_keys == 0) {
+        lse[r] = -INFINITY;
+        continue;
+      }
       /* scores s_j = scale * <q_i, k_j> */
-      for (int64_t j = 0; j < s_kv; ++j) {
+      for (int64_t j = 0; j < n_keys; ++j) {
         double dot = 0.0;
         for (int64_t e = 0; e < d; ++e) dot += qi[e] * kb[j * d + e];
         s[j] = scale * dot;
       }
       double m = s[0];
-      for (int64_t j = 1; j < s_kv; ++j)
+      for (int64_t j = 1; j < n_keys; ++j)
         if (s[j] > m) m = s[j];
       double z = 0.0;
-      for (int64_t j = 0; j < s_kv; ++j) z += exp(s[j] - m);
-      double* oi = out + r * d;
-      for (int64_t e = 0; e < d; ++e) oi[e] = 0.0;
-      for (int64_t j = 0; j < s_kv; ++j) {
+      for (int64_t j = 0; j < n_keys; ++j) z += exp(s[j] - m);
+      for (int64_t j = 0; j < n_keys; ++j) {
         double w = exp(s[j] - m) / z;
         for (int64_t e = 0; e < d; ++e) oi[e] += w * vb[j * d + e];
       }
@@ -91,34 +101,44 @@ int cpo_attention_rows(const double* q, const double* k, const double* v,
  *    only, emitting the partial output and its fp32-able LSE ([API]
  *    convert_to_fp32: "output and LSE").  Deliberately a separate routine from
  *    (1): two passes over the keys, scores recomputed in the second pass, the
- *    normalisation applied once at the end.
+ *    normalisation applied once at the end.  causal != 0: only keys
+ *    j <= i of the range count; a row left with none gives the empty partial
+ *    (0, -inf), which the merge below treats as its identity.
  * ------------------------------------------------------------------------- */
 int cpo_partial_rows(const double* q, const double* k, const double* v,
                      int64_t nbh, int64_t s_q, int64_t s_kv, int64_t d,
                      double scale, int64_t k0, int64_t k1,
                      const int64_t* row_ids, int64_t n_rows,
-                     double* out, double* lse) {
+                     double* out, double* lse, int causal) {
   if (k0 < 0 || k1 > s_kv || k1 <= k0) return CPO_ERR_SHAPE;
   if (row_ids == NULL) n_rows = nbh * s_q;
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < n_rows; ++r) {
     int64_t row = row_ids ? row_ids[r] : r;
     int64_t bh = row / s_q;
+    int64_t i = row % s_q;
     const double* qi = q + row * d;
     const double* kb = k + bh * s_kv * d;
     const double* vb = v + bh * s_kv * d;
+    int64_t hi_key = k1;
+    if (causal && i + 1 < k1) hi_key = i + 1;
+    double* oi = out + r * d;
+    if (hi_key <= k0) {
+      for (int64_t e = 0; e < d; ++e) oi[e] = 0.0;
+      lse[r] = -INFINITY;
+      continue;
+    }
     /* pass 1: the largest score in the range */
     double m = -INFINITY;
-    for (int64_t j = k0; j < k1; ++j) {
+    for (int64_t j = k0; j < hi_key; ++j) {
       double dot = 0.0;
       for (int64_t e = 0; e < d; ++e) dot += qi[e] * kb[j * d + e];
       if (scale * dot > m) m = scale * dot;
     }
     /* pass 2: unnormalised weights, their sum and the weighted V rows */
-    double* oi = out + r * d;
     for (int64_t e = 0; e < d; ++e) oi[e] = 0.0;
     double z = 0.0;
-    for (int64_t j = k0; j < k1; ++j) {
+    for (int64_t j = k0; j < hi_key; ++j) {
       double dot = 0.0;
       for (int64_t e = 0; e < d; ++e) dot += qi[e] * kb[j * d + e];
       double p = exp(scale * dot - m);
@@ -191,7 +211,7 @@ int cpo_ring_rows(const double* q, const double* k, const double* v,
                   int64_t nbh, int64_t s_q, int64_t s_kv, int64_t d,
                   double scale, int64_t ring_degree, int ring_anything,
                   const int64_t* row_ids, int64_t n_rows,
-                  double* out, double* lse) {
+                  double* out, double* lse, int causal) {
   if (ring_degree < 1) return CPO_ERR_SHAPE;
   int64_t* bounds = (int64_t*)malloc((size_t)(ring_degree + 1) * sizeof(int64_t));
   if (bounds == NULL) return CPO_ERR_ALLOC;
@@ -208,10 +228,10 @@ int cpo_ring_rows(const double* q, const double* k, const double* v,
     return CPO_ERR_ALLOC;
   }
   rc = cpo_partial_rows(q, k, v, nbh, s_q, s_kv, d, scale, bounds[0], bounds[1],
-                        row_ids, n_rows, out, lse);
+                        row_ids, n_rows, out, lse, causal);
   for (int64_t c = 1; c < ring_degree && rc == CPO_OK; ++c) {
     rc = cpo_partial_rows(q, k, v, nbh, s_q, s_kv, d, scale, bounds[c],
-                          bounds[c + 1], row_ids, n_rows, o_c, l_c);
+                          bounds[c + 1], row_ids, n_rows, o_c, l_c, causal);
     if (rc == CPO_OK) cpo_merge(out, lse, o_c, l_c, n_rows, d);
   }
   free(bounds); free(o_c); free(l_c);

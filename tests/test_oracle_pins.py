@@ -259,6 +259,47 @@ def pin_unified_is_full_attention():
         assert np.allclose(lg, rl, atol=1e-12)
 
 
+# --------------------------------------------------------------------------
+# causal (scaled_dot_product_attention's is_causal: query i attends keys j <= i)
+# --------------------------------------------------------------------------
+def pin_causal_torch_crosscheck():
+    for (lead, s_q, s_kv, d) in [((2,), 7, 7, 3), ((1, 3), 12, 12, 5), ((2,), 5, 9, 4),
+                                 ((1,), 9, 4, 2)]:
+        q, k, v = _rand(*lead, s_q, d), _rand(*lead, s_kv, d), _rand(*lead, s_kv, d)
+        o, l = oracle.attention(q, k, v, 0.45, causal=True)
+        qt, kt, vt = (torch.from_numpy(x) for x in (q, k, v))
+        sc = 0.45 * (qt @ kt.transpose(-1, -2))
+        allowed = torch.ones(s_q, s_kv, dtype=torch.bool).tril()     # top-left aligned
+        sc = sc.masked_fill(~allowed, float("-inf"))
+        ro = torch.softmax(sc, dim=-1) @ vt
+        rl = torch.logsumexp(sc, dim=-1)
+        assert np.allclose(o, ro.numpy(), atol=1e-12) and np.allclose(l, rl.numpy(), atol=1e-12)
+
+
+def pin_causal_closed_forms():
+    q, k, v = _rand(2, 6, 4), _rand(2, 6, 4), _rand(2, 6, 4)
+    o, l = oracle.attention(q, k, v, 0.8, causal=True)
+    # the first query sees only the first key
+    assert np.allclose(o[:, 0], v[:, 0], atol=1e-15)
+    assert np.allclose(l[:, 0], 0.8 * np.einsum("bd,bd->b", q[:, 0], k[:, 0]), atol=1e-14)
+    # the last query of a square problem sees every key: plain attention
+    fo, fl = oracle.attention(q, k, v, 0.8)
+    assert np.allclose(o[:, -1], fo[:, -1], atol=1e-14) and np.allclose(l[:, -1], fl[:, -1], atol=1e-14)
+    # a key range entirely after a row gives that row the empty partial
+    po, pl = oracle.partial(q, k, v, 0.8, 3, 6, causal=True)
+    assert np.all(po[:, :3] == 0) and np.all(pl[:, :3] == -np.inf)
+    assert np.all(np.isfinite(pl[:, 3:]))
+
+
+def pin_causal_ring_equals_full():
+    s = 19
+    q, k, v = _rand(2, s, 6), _rand(2, s, 6), _rand(2, s, 6)
+    ro, rl = oracle.attention(q, k, v, 0.5, causal=True)
+    for r in range(1, s + 1):
+        o, l = oracle.ring(q, k, v, 0.5, ring_degree=r, ring_anything=True, causal=True)
+        assert np.allclose(o, ro, atol=1e-12) and np.allclose(l, rl, atol=1e-12), r
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
@@ -286,6 +327,9 @@ MUTANTS = {
     "uneven_extra_at_end": ("bounds[c + 1] = bounds[c] + base + (c < extra ? 1 : 0);",
                             "bounds[c + 1] = bounds[c] + base + (c >= ring_degree - extra ? 1 : 0);"),
     "even_split_not_checked": ("if (!ring_anything && s_kv % ring_degree != 0) return CPO_ERR_DIVISIBILITY;", ""),
+    "causal_excludes_diagonal": ("if (causal && i + 1 < s_kv) n_keys = i + 1;",
+                                 "if (causal && i < s_kv) n_keys = i;"),
+    "partial_causal_ignored": ("if (causal && i + 1 < k1) hi_key = i + 1;", ""),
     "permute_group_index": ("int64_t bshd = ((bi * s + si) * h + gi * hg + hh) * d + e;",
                             "int64_t bshd = ((bi * s + si) * h + hh * g + gi) * d + e;"),
 }
