@@ -196,7 +196,8 @@ def ring_workload_step(name, dev):
     ws = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
 
     def step():
-        cp.ring(q, k, v, w.ring_degree, w.ring_anything, out=out, lse=lse, workspace=ws)
+        cp.ring(q, k, v, w.ring_degree, w.ring_anything, out=out, lse=lse, workspace=ws,
+                causal=w.causal)
     return w, step, (q, k, v, out, lse, ws)
 
 
@@ -328,7 +329,7 @@ def aux_measurements(dev, stream, peaks):
                               "timing": "80 calls in one CUDA graph over 8 rotating sets > L2"}
     del xs, ys
     # the other attention workloads
-    for name in ("uneven_ring", "video_ring", "tiny_ring"):
+    for name in ("uneven_ring", "video_ring", "tiny_ring", "flux_ring_causal"):
         w, step, keep = ring_workload_step(name, dev)
         for _ in range(3):
             step()

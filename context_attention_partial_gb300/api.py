@@ -75,8 +75,10 @@ def ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ring_degree: int = 1
          ring_anything: bool = False, scale: Optional[float] = None,
          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
          workspace: Optional[torch.Tensor] = None,
-         stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+         stream: Optional[torch.cuda.Stream] = None,
+         causal: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
     """The ring schedule on one GPU: q [B,H,S_q,D], k, v [B,H,S_kv,D].
+    causal: query i attends keys j <= i (cpattn_ring_causal).
     Returns (out [B,H,S_q,D] in q's dtype, lse f32 [B,H,S_q])."""
     lib = _lib.load()
     B, H, S, D = q.shape
@@ -90,8 +92,10 @@ def ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ring_degree: int = 1
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     dq, dk, dv, do, dl = _desc(q), _desc(k), _desc(v), _desc(out), _desc(lse)
-    check(lib.cpattn_ring(dq, dk, dv, _scale(scale), int(ring_degree), int(bool(ring_anything)),
-                          do, dl, ws_ptr, ws_bytes, _stream_handle(stream)), "cpattn_ring")
+    fn = lib.cpattn_ring_causal if causal else lib.cpattn_ring
+    check(fn(dq, dk, dv, _scale(scale), int(ring_degree), int(bool(ring_anything)),
+             do, dl, ws_ptr, ws_bytes, _stream_handle(stream)),
+          "cpattn_ring_causal" if causal else "cpattn_ring")
     return out, lse
 
 
@@ -148,7 +152,8 @@ def grouped_as_bhsd(t: torch.Tensor) -> torch.Tensor:
 def unified_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ulysses_degree: int,
                       ring_degree: int = 1, scale: Optional[float] = None,
                       stream: Optional[torch.cuda.Stream] = None,
-                      buffers: Optional[dict] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                      buffers: Optional[dict] = None,
+                      causal: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
     """Unified (Ulysses x Ring) attention on one GPU (Diffusers "Context
     parallelism", "Unified Attention": an all-to-all regroups heads and
     tokens, Ring Attention runs on the result, the all-to-all is reversed).
@@ -179,7 +184,7 @@ def unified_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ulysses
     need = ring_workspace_bytes(qv, R)
     ws = buf("ws", (max(need, 16),), torch.uint8) if need > 0 else None
     ring(qv, grouped_as_bhsd(kg), grouped_as_bhsd(vg), R, False, scale,
-         out=grouped_as_bhsd(og), lse=lse, workspace=ws, stream=stream)
+         out=grouped_as_bhsd(og), lse=lse, workspace=ws, stream=stream, causal=causal)
     out = ulysses_permute(og, G, -1, out=buf("out", (B, S, H, D), q.dtype), stream=stream)
     return out, lse
 

@@ -127,18 +127,30 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int b, int rows) {
 }
 
 // Walks the (chunk, tile) sequence shared by all roles.
+// The key tiles of chunk c this CTA visits: all of them, or with causal
+// masking only those starting at or before `kmax`, the CTA's last query row.
+__device__ __forceinline__ int chunk_tiles(const AttnParams& p, int c, int kmax) {
+  const int end = min(p.chunk_start[c + 1], kmax + 1);
+  return end > p.chunk_start[c] ? ceil_div(end - p.chunk_start[c], kBN) : 0;
+}
+
+// Walks the (chunk, tile) sequence shared by all roles; r_eff chunks (with
+// causal masking the chunks past the CTA's last query row are empty for
+// every row here, identities of the merge, and are not visited).
 struct TileWalk {
-  int c = 0, t = 0, nt = 0;
-  __device__ void start(const AttnParams& p) {
+  int c = 0, t = 0, nt = 0, kmax = 0, r_eff = 0;
+  __device__ void start(const AttnParams& p, int kmax_, int r_eff_) {
     c = 0;
     t = 0;
-    nt = ceil_div(p.chunk_start[1] - p.chunk_start[0], kBN);
+    kmax = kmax_;
+    r_eff = r_eff_;
+    nt = chunk_tiles(p, 0, kmax);
   }
   __device__ void next(const AttnParams& p) {
     if (++t == nt) {
       ++c;
       t = 0;
-      if (c < p.ring_degree) nt = ceil_div(p.chunk_start[c + 1] - p.chunk_start[c], kBN);
+      if (c < r_eff) nt = chunk_tiles(p, c, kmax);
     }
   }
 };
@@ -161,11 +173,14 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float factor) {
 // (o_c = O / l, lse_c = m ln2 + ln l) and fold it into the running result.
 template <typename T, int D>
 __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO, int c,
-                                               float m_used, float l, int b, int h, int q_row,
-                                               bool row_ok) {
-  const bool last = (c == p.ring_degree - 1);
-  const float inv_l = 1.0f / l;
-  const float lse_c = (m_used + log2f(l)) * kLn2;
+                                               int r_eff, float m_used, float l, int b, int h,
+                                               int q_row, bool row_ok) {
+  const bool last = (c == r_eff - 1);
+  // a row with no admissible key in the chunk (causal masking) emits the
+  // empty partial (0, -inf): the identity of the merge below
+  const bool empty = !(l > 0.f);
+  const float inv_l = empty ? 0.f : 1.0f / l;
+  const float lse_c = empty ? -INFINITY : (m_used + log2f(l)) * kLn2;
   const int64_t flat = (static_cast<int64_t>(b) * p.heads + h) * p.s_q + q_row;
   float w_run = 0.f, w_c = 1.f, lse_new = lse_c;
   if (c > 0 && row_ok) {
@@ -228,7 +243,7 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
   __syncwarp();
 }
 
-template <typename T, int D>
+template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -265,8 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int q_row0 = blockIdx.x * (kNT * kBM);
-  const int h = blockIdx.y, b = blockIdx.z;
+  // causal: grid (H, B, query blocks), the heaviest query blocks first
+  const int q_row0 =
+      (CAUSAL ? static_cast<int>(gridDim.z - 1 - blockIdx.z) : static_cast<int>(blockIdx.x)) *
+      (kNT * kBM);
+  const int h = CAUSAL ? blockIdx.x : blockIdx.y;
+  const int b = CAUSAL ? blockIdx.y : blockIdx.z;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR_Q, 1);
@@ -304,9 +323,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
+  // largest key index a row of this CTA may attend; chunks starting past it
+  // are skipped (chunk 0 starts at key 0, so at least one chunk remains)
+  // (INT_MAX - 1 without causal masking, so that kmax + 1 cannot overflow)
+  const int kmax = CAUSAL ? min(q_row0 + kNT * kBM, p.s_q) - 1 : 0x7ffffffe;
+  int r_eff = p.ring_degree;
+  if (CAUSAL)
+    while (r_eff > 1 && p.chunk_start[r_eff - 1] > kmax) --r_eff;
   int n_tiles = 0;
-  for (int c = 0; c < p.ring_degree; ++c)
-    n_tiles += ceil_div(p.chunk_start[c + 1] - p.chunk_start[c], kBN);
+  for (int c = 0; c < r_eff; ++c) n_tiles += chunk_tiles(p, c, kmax);
 
   if (warp >= 8) {
     regs_decrease<kControlRegs>();
@@ -334,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bounded wait runs out and the CTA takes the abort path
       bool ok = p.fault_skip_kv == 0;
       TileWalk w;
-      w.start(p);
+      w.start(p, kmax, r_eff);
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int key0 = p.chunk_start[w.c] + w.t * kBN;
         for (int which = 0; which < 2; ++which) {
@@ -419,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       TileWalk w;
-      w.start(p);
+      w.start(p, kmax, r_eff);
       for (int j = 0; j < n_tiles && ok; ++j) {
         const uint32_t acc = w.t != 0 ? 1u : 0u;
         const int lv = 2 * j + 1, sv = lv % C::STAGES;
@@ -576,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     TileWalk w;
-    w.start(p);
+    w.start(p, kmax, r_eff);
     for (int j = 0; j < n_tiles && ok; ++j) {
       ok = mbar_wait(bar_s(wg), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error,
                      kErrWaitSoftmax);
@@ -584,12 +609,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (w.t == 0 && w.c > 0)
-        chunk_epilogue<T, D>(p, tO, w.c - 1, m_used, l, b, h, q_row, row_ok);
+        chunk_epilogue<T, D>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok);
 
       uint32_t s[kBN];
       tmem_ld_x128(tS, s);
-      const int valid = p.chunk_start[w.c + 1] - (p.chunk_start[w.c] + w.t * kBN);
-      if (valid < kBN) {
+      // keys past the chunk's end, and with causal masking keys after this
+      // row, are masked
+      const int key0 = p.chunk_start[w.c] + w.t * kBN;
+      int valid = p.chunk_start[w.c + 1] - key0;
+      if constexpr (CAUSAL) valid = min(valid, q_row + 1 - key0);
+      if (CAUSAL ? __any_sync(0xffffffffu, valid < kBN) : valid < kBN) {
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
           if (i >= valid) s[i] = f2u(-INFINITY);
@@ -619,7 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (__any_sync(0xffffffffu, need)) rescale_o<D>(tO, factor);
 
-      const float neg_m = -m_used;
+      // a row with every key so far masked keeps m = -inf; its P stays 0
+      const float neg_m = (CAUSAL && m_used == -INFINITY) ? 0.f : -m_used;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < kBN / 2; ++i) {
@@ -653,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        chunk_epilogue<T, D>(p, tO, p.ring_degree - 1, m_used, l, b, h, q_row, row_ok);
+        chunk_epilogue<T, D>(p, tO, r_eff - 1, r_eff, m_used, l, b, h, q_row, row_ok);
       }
     }
   }
@@ -666,11 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool CAUSAL>
 cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                         const AttnParams& p, cudaStream_t stream) {
   using C = Cfg<T, D>;
-  auto kernel = attn_fwd_kernel<T, D>;
+  auto kernel = attn_fwd_kernel<T, D, CAUSAL>;
   // The setmaxnreg split assumes exactly kLaunchRegs registers per thread at
   // launch; with fewer, the softmax warpgroups' increase could never be
   // granted.  Refuse to launch such a build.
@@ -680,7 +710,8 @@ cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
   if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.s_q + kNT * kBM - 1) / (kNT * kBM), p.heads, p.batch);
+  const unsigned q_blocks = (p.s_q + kNT * kBM - 1) / (kNT * kBM);
+  const dim3 grid = CAUSAL ? dim3(p.heads, p.batch, q_blocks) : dim3(q_blocks, p.heads, p.batch);
   kernel<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
@@ -690,12 +721,16 @@ cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
 cudaError_t launch_attention(InDtype dt, int head_dim, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const AttnParams& p, cudaStream_t stream) {
+  const bool c = p.causal != 0;
   if (dt == InDtype::BF16 && head_dim == 128)
-    return launch_impl<__nv_bfloat16, 128>(tm_q, tm_k, tm_v, p, stream);
+    return c ? launch_impl<__nv_bfloat16, 128, true>(tm_q, tm_k, tm_v, p, stream)
+             : launch_impl<__nv_bfloat16, 128, false>(tm_q, tm_k, tm_v, p, stream);
   if (dt == InDtype::BF16 && head_dim == 64)
-    return launch_impl<__nv_bfloat16, 64>(tm_q, tm_k, tm_v, p, stream);
+    return c ? launch_impl<__nv_bfloat16, 64, true>(tm_q, tm_k, tm_v, p, stream)
+             : launch_impl<__nv_bfloat16, 64, false>(tm_q, tm_k, tm_v, p, stream);
   if (dt == InDtype::F32 && head_dim == 64)
-    return launch_impl<float, 64>(tm_q, tm_k, tm_v, p, stream);
+    return c ? launch_impl<float, 64, true>(tm_q, tm_k, tm_v, p, stream)
+             : launch_impl<float, 64, false>(tm_q, tm_k, tm_v, p, stream);
   return cudaErrorInvalidValue;
 }
 

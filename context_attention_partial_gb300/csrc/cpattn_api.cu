@@ -150,7 +150,7 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
                             const cpattn_tensor* v, float scale, int ring_degree,
                             int ring_anything, cpattn_tensor* out, cpattn_tensor* lse,
                             void* workspace, size_t workspace_bytes, bool out_f32,
-                            cudaStream_t stream) {
+                            bool causal, cudaStream_t stream) {
   cpattn_status st = check_qkv(q, k, v);
   if (st != CPATTN_OK) return st;
   if (!out || !lse) return CPATTN_ERR_NULL;
@@ -216,6 +216,7 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   p.out_f32 = out->dtype == CPATTN_F32 ? 1 : 0;
   p.timeout_ns = g_timeout_ns.load();
   p.fault_skip_kv = g_fault_skip_kv.load();
+  p.causal = causal ? 1 : 0;
   for (int c = 0; c <= ring_degree; ++c) p.chunk_start[c] = chunk_start[c];
   const cudaError_t e =
       cpattn::launch_attention(q->dtype == CPATTN_BF16 ? InDtype::BF16 : InDtype::F32,
@@ -230,7 +231,7 @@ extern "C" {
 cpattn_status cpattn_partial(const cpattn_tensor* q, const cpattn_tensor* k,
                              const cpattn_tensor* v, float scale, cpattn_tensor* out,
                              cpattn_tensor* lse, void* stream) {
-  return run_attention(q, k, v, scale, 1, 0, out, lse, nullptr, 0, true,
+  return run_attention(q, k, v, scale, 1, 0, out, lse, nullptr, 0, true, false,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -239,7 +240,15 @@ cpattn_status cpattn_ring(const cpattn_tensor* q, const cpattn_tensor* k, const 
                           cpattn_tensor* lse, void* workspace, size_t workspace_bytes,
                           void* stream) {
   return run_attention(q, k, v, scale, ring_degree, ring_anything, out, lse, workspace,
-                       workspace_bytes, false, static_cast<cudaStream_t>(stream));
+                       workspace_bytes, false, false, static_cast<cudaStream_t>(stream));
+}
+
+cpattn_status cpattn_ring_causal(const cpattn_tensor* q, const cpattn_tensor* k,
+                                 const cpattn_tensor* v, float scale, int ring_degree,
+                                 int ring_anything, cpattn_tensor* out, cpattn_tensor* lse,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  return run_attention(q, k, v, scale, ring_degree, ring_anything, out, lse, workspace,
+                       workspace_bytes, false, true, static_cast<cudaStream_t>(stream));
 }
 
 size_t cpattn_ring_workspace_bytes(const cpattn_tensor* q, int ring_degree) {

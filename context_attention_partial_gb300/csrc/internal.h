@@ -24,6 +24,7 @@ struct AttnParams {
   int out_f32;           // 1: out is f32, 0: out has the input dtype (bf16)
   unsigned long long timeout_ns;
   int fault_skip_kv;     // testing: the producer issues no K/V loads
+  int causal;            // 1: query i attends keys j <= i (is_causal)
   int chunk_start[CPATTN_MAX_RING_DEGREE + 1];
 };
 

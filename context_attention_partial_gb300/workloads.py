@@ -32,6 +32,7 @@ class Workload:
     ulysses_degree: int = 1
     layout: str = "bhsd"     # "bhsd": [B, H, S, D]; "bshd": [B, S, H, D]
     description: str = ""
+    causal: bool = False     # query i attends keys j <= i
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -45,9 +46,10 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """4 * B * H * S_q * S_kv * D: Q K^T plus P V, non-causal, exp not
-        counted, no padding counted."""
-        return 4.0 * self.batch * self.heads * self.seq * self.seq * self.head_dim
+        """4 * B * H * D * (query, key) pairs: Q K^T plus P V, exp not
+        counted, no padding counted; S^2 pairs, or S (S + 1) / 2 causal."""
+        pairs = self.seq * (self.seq + 1) / 2 if self.causal else self.seq * self.seq
+        return 4.0 * self.batch * self.heads * pairs * self.head_dim
 
 
 WORKLOADS = {
@@ -66,6 +68,9 @@ WORKLOADS = {
         Workload("uneven_ring", 2, 24, 4609, 128, "bf16", ring_degree=3, ring_anything=True,
                  description="ring_anything uneven split: bf16 [2,24,4609,128], "
                              "ring_degree 3"),
+        Workload("flux_ring_causal", 1, 24, 4608, 128, "bf16", ring_degree=2, causal=True,
+                 description="FLUX-like shape with causal masking: bf16 [1,24,4608,128], "
+                             "ring_degree 2, is_causal"),
         Workload("unified", 1, 24, 4608, 128, "bf16", ring_degree=2, ulysses_degree=2,
                  layout="bshd",
                  description="Unified (Ulysses x Ring) on the FLUX-like shape: bf16 "

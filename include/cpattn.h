@@ -136,6 +136,22 @@ cpattn_status cpattn_ring(const cpattn_tensor* q, const cpattn_tensor* k,
                           size_t workspace_bytes, void* stream);
 
 /*
+ * cpattn_ring_causal -- cpattn_ring with causal masking, the is_causal of
+ * scaled_dot_product_attention ([PARA] passes is_causal; SDPA's mask is
+ * top-left aligned): query i attends keys j <= i only.  Every chunk's
+ * partial covers the admissible keys of that chunk; a row with none gets the
+ * empty partial (0, -inf), the identity of the merge, so the ring result is
+ * causal attention over all keys.  Chunks wholly after a query tile are not
+ * visited, and query tiles are scheduled heaviest first.  Arguments, layout,
+ * workspace and errors as cpattn_ring.
+ */
+cpattn_status cpattn_ring_causal(const cpattn_tensor* q, const cpattn_tensor* k,
+                                 const cpattn_tensor* v, float scale, int ring_degree,
+                                 int ring_anything, cpattn_tensor* out,
+                                 cpattn_tensor* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * cpattn_ulysses_permute -- the Ulysses head regroup ([CP] "Ulysses
  * Attention": the all-to-all leaves each of G ranks every token for H/G
  * heads), on one GPU a bit-exact layout permute:

@@ -260,3 +260,42 @@ def test_unified_matches_oracle(b, s, h, d, g, r, dt):
     assert out.shape == q.shape and out.dtype == dt
     assert maxabs(out, ro) <= to
     assert maxabs(lse.reshape(g, b, h // g, s), rl) <= tl
+
+
+CAUSAL_CASES = [
+    # (B, H, S_q, S_kv, D, dtype, R, anything)
+    (1, 2, 300, 300, 128, torch.bfloat16, 3, False),
+    (1, 2, 301, 301, 128, torch.bfloat16, 3, True),      # 101/100/100
+    (2, 2, 129, 1000, 128, torch.bfloat16, 5, False),    # S_q < S_kv: top-left aligned
+    (1, 3, 256, 256, 64, torch.bfloat16, 4, False),
+    (1, 2, 513, 513, 128, torch.bfloat16, 5, True),
+    (1, 1, 700, 700, 128, torch.bfloat16, 1, False),
+    (1, 2, 256, 256, 64, torch.float32, 4, False),
+    (1, 1, 77, 13, 128, torch.bfloat16, 13, True),
+]
+
+
+@pytest.mark.parametrize("case", CAUSAL_CASES, ids=lambda c: "x".join(map(str, c[:5])) + f"R{c[6]}{'a' if c[7] else ''}{str(c[5])[-4:]}")
+def test_ring_causal_matches_oracle(case):
+    B, H, Sq, Skv, D, dt, R, anything = case
+    g = torch.Generator("cpu").manual_seed(41)
+    q = torch.randn(B, H, Sq, D, generator=g).to(dt)
+    k = torch.randn(B, H, Skv, D, generator=g).to(dt)
+    v = torch.randn(B, H, Skv, D, generator=g).to(dt)
+    out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=R, ring_anything=anything,
+                       causal=True)
+    torch.cuda.synchronize()
+    status_ok()
+    ro, rl = oracle.ring(q, k, v, D ** -0.5, ring_degree=R, ring_anything=anything, causal=True)
+    to, tl = TOL[dt]
+    assert maxabs(out, ro) <= to
+    assert maxabs(lse, rl) <= tl
+
+
+def test_unified_causal_matches_oracle():
+    q, k, v = make_qkv((1, 300, 8, 128), torch.bfloat16, seed=43)
+    out, lse = cp.unified_attention(q.to(DEV), k.to(DEV), v.to(DEV), 2, 3, causal=True)
+    torch.cuda.synchronize()
+    ro, rl = oracle.unified(q, k, v, 2, 3, 128 ** -0.5, causal=True)
+    assert maxabs(out, ro) <= 1e-2
+    assert maxabs(lse.reshape(2, 1, 4, 300), rl) <= 1e-3

@@ -38,7 +38,8 @@ def check_convex(out, v, dims):
 def run_ring_workload(name, heads_to_check):
     w, q, k, v = make_workload(name, seed=0)
     gq, gk, gv = q.to(DEV), k.to(DEV), v.to(DEV)
-    out, lse = cp.ring(gq, gk, gv, ring_degree=w.ring_degree, ring_anything=w.ring_anything)
+    out, lse = cp.ring(gq, gk, gv, ring_degree=w.ring_degree, ring_anything=w.ring_anything,
+                       causal=w.causal)
     torch.cuda.synchronize()
     assert cp.last_device_status() == 0
     assert out.dtype == q.dtype and lse.dtype == torch.float32
@@ -48,9 +49,16 @@ def run_ring_workload(name, heads_to_check):
     out_c, lse_c = out.cpu(), lse.cpu()
     for i, (b, h) in enumerate(heads_to_check):
         rows = sample_rows(w.seq, i)
-        ro, rl = oracle.ring(q[b, h, rows].unsqueeze(0), k[b, h].unsqueeze(0), v[b, h].unsqueeze(0),
-                             w.head_dim ** -0.5, ring_degree=w.ring_degree,
-                             ring_anything=w.ring_anything)
+        if w.causal:
+            # causal rows depend on their position: evaluate whole-sequence rows
+            ro, rl = oracle.ring(q[b, h].unsqueeze(0), k[b, h].unsqueeze(0), v[b, h].unsqueeze(0),
+                                 w.head_dim ** -0.5, ring_degree=w.ring_degree,
+                                 ring_anything=w.ring_anything, causal=True, rows=rows)
+            ro, rl = ro[None], rl[None]
+        else:
+            ro, rl = oracle.ring(q[b, h, rows].unsqueeze(0), k[b, h].unsqueeze(0),
+                                 v[b, h].unsqueeze(0), w.head_dim ** -0.5,
+                                 ring_degree=w.ring_degree, ring_anything=w.ring_anything)
         go = out_c[b, h, rows].float().numpy()
         gl = lse_c[b, h, rows].numpy()
         assert np.abs(go - ro[0]).max() <= tol_o, (name, b, h)
@@ -73,6 +81,10 @@ def test_flux_ring_sampled():
 
 def test_uneven_ring_sampled():
     run_ring_workload("uneven_ring", [(0, 0), (1, 7), (1, 23)])
+
+
+def test_flux_ring_causal_sampled():
+    run_ring_workload("flux_ring_causal", [(0, 0), (0, 13), (0, 23)])
 
 
 @pytest.mark.slow
