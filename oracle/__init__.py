@@ -26,6 +26,12 @@ Functions and the passages they follow (page title, section):
 * ``unified``     -- Diffusers "Context parallelism", "Unified Attention":
   regroup, ring within each group, inverse regroup (composition of the
   functions above).
+* ``ulysses_anything_heads`` / ``ulysses_anything_permute`` /
+  ``ulysses_anything`` -- Diffusers "Context parallelism", "Ulysses Anything
+  Attention" (and the ``ulysses_anything`` parameter of the "Parallelism"
+  API): the regroup without divisibility, heads dealt out with tensor_split
+  rules into groups padded to ceil(H/G) slots; attention per group on its
+  own heads; inverse regroup.
 """
 from __future__ import annotations
 
@@ -72,9 +78,12 @@ def _bind(path: str):
     lib.cpo_chunk_bounds.argtypes = [i64, i64, ctypes.c_int, p]
     lib.cpo_ring_rows.argtypes = [p, p, p, i64, i64, i64, i64, d, i64, ctypes.c_int, p, i64, p, p, ci]
     lib.cpo_ulysses_permute.argtypes = [p, p, i64, i64, i64, i64, i64, ctypes.c_int, i64]
+    lib.cpo_ulysses_anything_heads.argtypes = [i64, i64, p]
+    lib.cpo_ulysses_anything_permute.argtypes = [p, p, i64, i64, i64, i64, i64, ctypes.c_int, i64]
     lib.cpo_num_threads.argtypes = []
     for name in ("cpo_attention_rows", "cpo_partial_rows", "cpo_chunk_bounds",
-                 "cpo_ring_rows", "cpo_ulysses_permute", "cpo_num_threads"):
+                 "cpo_ring_rows", "cpo_ulysses_permute", "cpo_ulysses_anything_heads",
+                 "cpo_ulysses_anything_permute", "cpo_num_threads"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -277,6 +286,85 @@ def unified(q, k, v, ulysses_degree: int, ring_degree: int = 1, scale=None, caus
     o, l = ring(to_bhsd(qg), to_bhsd(kg), to_bhsd(vg), scale, ring_degree=R, causal=causal)
     og = np.ascontiguousarray(np.transpose(o, (0, 1, 3, 2, 4)))        # [G, B, S, Hg, D]
     return ulysses_permute(og, G, -1), l
+
+
+def ulysses_anything_heads(heads: int, degree: int):
+    """Head groups of Ulysses Anything: group g holds heads
+    [start[g], start[g+1]); returns start (length degree + 1)."""
+    start = np.zeros(int(degree) + 1, dtype=np.int64)
+    _check(_load().cpo_ulysses_anything_heads(int(heads), int(degree), _ptr(start)))
+    return [int(x) for x in start]
+
+
+def _raw(x):
+    if hasattr(x, "detach"):
+        import torch
+        t = x.detach().cpu().contiguous()
+        if t.element_size() == 2:
+            return t.view(torch.int16).numpy()
+        if t.element_size() == 4:
+            return t.view(torch.int32).numpy()
+        return t.numpy()
+    return np.ascontiguousarray(x)
+
+
+def ulysses_anything_permute(x, degree: int, direction: int, heads: int = None, fill=0):
+    """Ulysses Anything regroup as a byte-exact layout permute.
+    direction +1: x [B, S, H, D] -> [G, B, S, ceil(H/G), D]; padding slots
+    hold ``fill``.  direction -1: x [G, B, S, ceil(H/G), D] -> [B, S, H, D];
+    ``heads`` = H is required (padding slots are never read)."""
+    raw = _raw(x)
+    G = int(degree)
+    if G < 1:
+        raise OracleError("the Ulysses degree must be >= 1")
+    if direction == 1:
+        if raw.ndim != 4:
+            raise OracleError("forward permute takes [B, S, H, D]")
+        b, s, h, d = raw.shape
+        out_shape = (G, b, s, -(-h // G), d)
+        y = np.full(out_shape, fill, dtype=raw.dtype)
+    elif direction == -1:
+        if raw.ndim != 5 or raw.shape[0] != G or heads is None:
+            raise OracleError("inverse permute takes [G, B, S, ceil(H/G), D] and H")
+        _, b, s, hm, d = raw.shape
+        h = int(heads)
+        if hm != -(-h // G):
+            raise OracleError("grouped tensor must have ceil(H/G) head slots")
+        y = np.empty((b, s, h, d), dtype=raw.dtype)
+    else:
+        raise OracleError("direction must be +1 or -1")
+    _check(_load().cpo_ulysses_anything_permute(_ptr(raw), _ptr(y), b, s, h, d, G, direction,
+                                                raw.dtype.itemsize))
+    if hasattr(x, "detach"):
+        import torch
+        yt = torch.from_numpy(y)
+        return yt.view(x.dtype) if yt.dtype != x.dtype else yt
+    return y
+
+
+def ulysses_anything(q, k, v, degree: int, scale=None, causal=False):
+    """Ulysses Anything attention as the steps of Diffusers "Context
+    parallelism", "Ulysses Anything Attention": regroup q, k, v [B, S, H, D]
+    into G head groups of tensor_split sizes (``ulysses_anything_permute``),
+    attention of every group over its own heads and the full sequence
+    (``attention``), inverse regroup.  Returns (out [B, S, H, D] float64,
+    lse [G, B, ceil(H/G), S] with NaN in the padding slots)."""
+    G = int(degree)
+    B, S, H, D = np.shape(q)
+    start = ulysses_anything_heads(H, G)
+    qg, kg, vg = (ulysses_anything_permute(_f64(x), G, 1) for x in (q, k, v))
+    hm = qg.shape[3]
+    og = np.zeros_like(qg)
+    lse = np.full((G, B, hm, S), np.nan)
+    for g in range(G):
+        hg = start[g + 1] - start[g]
+        if hg == 0:
+            continue
+        to_bhsd = lambda t: np.ascontiguousarray(np.transpose(t[g, :, :, :hg], (0, 2, 1, 3)))
+        o, l = attention(to_bhsd(qg), to_bhsd(kg), to_bhsd(vg), scale, causal=causal)
+        og[g, :, :, :hg] = np.transpose(o, (0, 2, 1, 3))
+        lse[g, :, :hg] = l
+    return ulysses_anything_permute(og, G, -1, heads=H), lse
 
 
 def num_threads() -> int:

@@ -12,9 +12,11 @@
  *
  * Sources (page title, section):
  *   [CP]   Diffusers "Context parallelism" guide: the variants table,
- *          "Ring Attention", "Ulysses Attention", "Ring Anything Attention".
+ *          "Ring Attention", "Ulysses Attention", "Ring Anything Attention",
+ *          "Ulysses Anything Attention".
  *   [API]  Diffusers "Parallelism" API page: ContextParallelConfig parameters
- *          ring_degree, ulysses_degree, convert_to_fp32, ring_anything.
+ *          ring_degree, ulysses_degree, convert_to_fp32, ring_anything,
+ *          ulysses_anything.
  *   [PARA] ParaAttention README, "Run Unified Attention ... with
  *          torch.compile": the sharded result must equal the matching slice of
  *          F.scaled_dot_product_attention (no mask, no dropout, not causal).
@@ -265,6 +267,61 @@ int cpo_ulysses_permute(const void* x, void* y, int64_t b, int64_t s,
             memcpy(dst + to * elem_bytes, src + from * elem_bytes,
                    (size_t)elem_bytes);
           }
+  return CPO_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * 7. Ulysses Anything ([CP] "Ulysses Anything Attention"; [API]
+ *    ulysses_anything): Ulysses without the requirement that H and S divide
+ *    by G (ring_degree stays 1).  The pages do not say how uneven heads are
+ *    dealt out; the reading taken is torch.tensor_split's: G consecutive
+ *    groups, the first H mod G of them one head longer.  On one device the
+ *    whole sequence lands in every group, so S needs no rule.
+ *
+ *    cpo_ulysses_anything_heads: start[0 .. G] with group g holding heads
+ *    [start[g], start[g+1]).
+ * ------------------------------------------------------------------------- */
+int cpo_ulysses_anything_heads(int64_t h, int64_t g, int64_t* start) {
+  if (g < 1 || h < 0) return CPO_ERR_SHAPE;
+  int64_t base = h / g, longer = h % g;
+  start[0] = 0;
+  for (int64_t i = 0; i < g; ++i)
+    start[i + 1] = start[i] + base + (i < longer ? 1 : 0);
+  return CPO_OK;
+}
+
+/*    cpo_ulysses_anything_permute: the regroup with every group padded to
+ *    hm = ceil(H/G) head slots (a reading: the exchange buffer must give all
+ *    groups one shape), group g filling slots 0 .. h_g - 1:
+ *      forward (dir = +1): y[g, b, s, j, :] = x[b, s, start[g] + j, :]
+ *                          for j < h_g; slots j >= h_g are not written.
+ *      inverse (dir = -1): y[b, s, start[g] + j, :] = x[g, b, s, j, :]
+ *                          for j < h_g; slots j >= h_g are not read.       */
+int cpo_ulysses_anything_permute(const void* x, void* y, int64_t b, int64_t s,
+                                 int64_t h, int64_t d, int64_t g, int dir,
+                                 int64_t elem_bytes) {
+  if (g < 1 || h < 1 || (dir != 1 && dir != -1)) return CPO_ERR_SHAPE;
+  int64_t hm = (h + g - 1) / g;
+  int64_t* start = (int64_t*)malloc((size_t)(g + 1) * sizeof(int64_t));
+  if (!start) return CPO_ERR_ALLOC;
+  cpo_ulysses_anything_heads(h, g, start);
+  const unsigned char* src = (const unsigned char*)x;
+  unsigned char* dst = (unsigned char*)y;
+  for (int64_t gi = 0; gi < g; ++gi) {
+    int64_t hg = start[gi + 1] - start[gi];
+    for (int64_t bi = 0; bi < b; ++bi)
+      for (int64_t si = 0; si < s; ++si)
+        for (int64_t j = 0; j < hg; ++j)
+          for (int64_t e = 0; e < d; ++e) {
+            int64_t bshd = ((bi * s + si) * h + start[gi] + j) * d + e;
+            int64_t grouped = (((gi * b + bi) * s + si) * hm + j) * d + e;
+            int64_t from = dir == 1 ? bshd : grouped;
+            int64_t to = dir == 1 ? grouped : bshd;
+            memcpy(dst + to * elem_bytes, src + from * elem_bytes,
+                   (size_t)elem_bytes);
+          }
+  }
+  free(start);
   return CPO_OK;
 }
 

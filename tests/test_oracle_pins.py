@@ -260,6 +260,69 @@ def pin_unified_is_full_attention():
 
 
 # --------------------------------------------------------------------------
+# Ulysses Anything (uneven head groups)
+# --------------------------------------------------------------------------
+def pin_ulysses_anything_heads():
+    for h, g, expect in read_golden("ulysses_anything_heads.txt"):
+        h, g = int(h), int(g)
+        if expect.startswith("ERR"):
+            with pytest.raises(oracle.OracleError):
+                oracle.ulysses_anything_heads(h, g)
+            continue
+        st = oracle.ulysses_anything_heads(h, g)
+        assert [st[i + 1] - st[i] for i in range(g)] == [int(x) for x in expect.split()], (h, g)
+    # library routine: numpy's array_split deals out the same groups
+    for h in range(1, 40):
+        for g in range(1, 12):
+            st = oracle.ulysses_anything_heads(h, g)
+            groups = np.array_split(np.arange(h), g)
+            assert st == [0] + list(np.cumsum([len(a) for a in groups]))
+
+
+def pin_ulysses_anything_permute():
+    for (b, s, h, d, g) in [(1, 5, 5, 3, 2), (2, 3, 7, 4, 3), (1, 4, 24, 2, 5), (1, 3, 24, 2, 7),
+                            (2, 2, 2, 3, 4), (1, 3, 6, 2, 3), (1, 2, 4, 8, 1)]:
+        x = RNG.integers(-2 ** 31, 2 ** 31 - 1, size=(b, s, h, d), dtype=np.int64).astype(np.int32)
+        y = oracle.ulysses_anything_permute(x, g, 1, fill=-7)
+        hm = -(-h // g)
+        assert y.shape == (g, b, s, hm, d)
+        # library routine: array_split of the head axis, each group padded
+        for gi, heads in enumerate(np.array_split(np.arange(h), g)):
+            assert np.array_equal(y[gi, :, :, :len(heads)], x[:, :, heads])
+            assert np.all(y[gi, :, :, len(heads):] == -7)
+        assert np.array_equal(oracle.ulysses_anything_permute(y, g, -1, heads=h), x)
+        if h % g == 0:   # no padding: plain Ulysses
+            assert np.array_equal(y, oracle.ulysses_permute(x, g, 1))
+    # padding slots are never read by the inverse
+    x = RNG.integers(0, 100, size=(1, 2, 5, 2)).astype(np.int32)
+    y = oracle.ulysses_anything_permute(x, 3, 1)
+    y[2, :, :, 1] = 12345
+    assert np.array_equal(oracle.ulysses_anything_permute(y, 3, -1, heads=5), x)
+    # bf16 through torch, bit-exact round trip
+    xt = torch.randn(2, 9, 7, 16).to(torch.bfloat16)
+    yt = oracle.ulysses_anything_permute(xt, 3, 1)
+    assert yt.dtype == torch.bfloat16 and tuple(yt.shape) == (3, 2, 9, 3, 16)
+    assert torch.equal(yt[2, :, :, :2], xt[:, :, 5:7])
+    assert torch.equal(oracle.ulysses_anything_permute(yt, 3, -1, heads=7), xt)
+
+
+def pin_ulysses_anything_is_full_attention():
+    """Every head keeps its full sequence in exactly one group, so the
+    composition is full attention per head, whatever the group sizes."""
+    for (b, s, h, d, g, causal) in [(1, 9, 5, 3, 2, False), (2, 7, 7, 4, 3, False),
+                                    (1, 6, 2, 2, 4, False), (1, 11, 5, 3, 3, True),
+                                    (1, 8, 6, 2, 3, False)]:
+        q, k, v = _rand(b, s, h, d), _rand(b, s, h, d), _rand(b, s, h, d)
+        o, l = oracle.ulysses_anything(q, k, v, g, 0.7, causal=causal)
+        bhsd = lambda t: np.transpose(t, (0, 2, 1, 3))
+        ro, rl = oracle.attention(bhsd(q), bhsd(k), bhsd(v), 0.7, causal=causal)
+        assert np.allclose(o, np.transpose(ro, (0, 2, 1, 3)), atol=1e-12)
+        for gi, heads in enumerate(np.array_split(np.arange(h), g)):
+            assert np.allclose(l[gi, :, :len(heads)], rl[:, heads], atol=1e-12)
+            assert np.all(np.isnan(l[gi, :, len(heads):]))
+
+
+# --------------------------------------------------------------------------
 # causal (scaled_dot_product_attention's is_causal: query i attends keys j <= i)
 # --------------------------------------------------------------------------
 def pin_causal_torch_crosscheck():
@@ -330,6 +393,12 @@ MUTANTS = {
     "causal_excludes_diagonal": ("if (causal && i + 1 < s_kv) n_keys = i + 1;",
                                  "if (causal && i < s_kv) n_keys = i;"),
     "partial_causal_ignored": ("if (causal && i + 1 < k1) hi_key = i + 1;", ""),
+    "anything_extra_heads_at_end": ("start[i + 1] = start[i] + base + (i < longer ? 1 : 0);",
+                                    "start[i + 1] = start[i] + base + (i >= g - longer ? 1 : 0);"),
+    "anything_dense_groups": ("int64_t grouped = (((gi * b + bi) * s + si) * hm + j) * d + e;",
+                              "int64_t grouped = (((gi * b + bi) * s + si) * hg + j) * d + e;"),
+    "anything_heads_reversed": ("int64_t bshd = ((bi * s + si) * h + start[gi] + j) * d + e;",
+                                "int64_t bshd = ((bi * s + si) * h + start[gi + 1] - 1 - j) * d + e;"),
     "permute_group_index": ("int64_t bshd = ((bi * s + si) * h + gi * hg + hh) * d + e;",
                             "int64_t bshd = ((bi * s + si) * h + hh * g + gi) * d + e;"),
 }
