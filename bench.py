@@ -26,6 +26,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -106,7 +108,7 @@ class ClockSampler:
     def summary(self):
         if not self.lines:
             return None
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, power = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -117,14 +119,22 @@ class ClockSampler:
                 mx = float(parts[2])
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
             for n, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(n)
         if not sm:
             return None
         loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if power:
+            out["power_w_median"] = statistics.median(power)
+            out["power_w_max"] = max(power)
+        return out
 
 
 def dist_setup(n_gpus: int):
@@ -202,16 +212,21 @@ def ring_workload_step(name, dev):
 
 
 def ulysses_step(dev, name="ulysses"):
-    """Ulysses (ring_degree 1) or Unified (ring_degree > 1) step: three
-    permutes, one attention launch over all head groups, one inverse permute."""
+    """Ulysses (ring_degree 1), Unified (ring_degree > 1) or Ulysses Anything
+    step: three permutes, one attention launch over all head groups, one
+    inverse permute."""
     import context_attention_partial_gb300 as cp
     from context_attention_partial_gb300.workloads import make_workload
     w, q, k, v = make_workload(name, seed=0)
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
     bufs = {}
 
-    def step():
-        cp.unified_attention(q, k, v, w.ulysses_degree, w.ring_degree, buffers=bufs)
+    if w.ulysses_anything:
+        def step():
+            cp.ulysses_anything_attention(q, k, v, w.ulysses_degree, buffers=bufs)
+    else:
+        def step():
+            cp.unified_attention(q, k, v, w.ulysses_degree, w.ring_degree, buffers=bufs)
     return w, step, (q, k, v, bufs)
 
 
@@ -327,6 +342,22 @@ def aux_measurements(dev, stream, peaks):
     aux["permute_ulysses"] = {"ms": ms, "GB/s": gbs, "bytes": nbytes,
                               "frac_hbm": gbs / peaks["hbm_gbs"],
                               "timing": "80 calls in one CUDA graph over 8 rotating sets > L2"}
+    # Ulysses Anything regroup (24 heads over 5 groups padded to 5 slots);
+    # padding slots are not written, so the bytes are the same as above
+    ys = [torch.empty(5, 1, 4608, 5, 128, device=dev, dtype=torch.bfloat16) for _ in range(8)]
+
+    def astep():
+        i = it[0] % 8
+        it[0] += 1
+        cp.ulysses_anything_permute(xs[i], 5, 1, out=ys[i])
+    for _ in range(5):
+        astep()
+    ms = time_graph(astep, 80, flush, stream)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    aux["permute_ulysses_anything"] = {"ms": ms, "GB/s": gbs, "bytes": nbytes,
+                                       "frac_hbm": gbs / peaks["hbm_gbs"],
+                                       "timing": "80 calls in one CUDA graph over 8 rotating "
+                                                 "sets > L2"}
     del xs, ys
     # the other attention workloads
     for name in ("uneven_ring", "video_ring", "tiny_ring", "flux_ring_causal"):
@@ -338,7 +369,7 @@ def aux_measurements(dev, stream, peaks):
         aux[name] = {"ms": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12,
                      "frac_bf16_peak": w.flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
         del keep
-    for name in ("ulysses", "unified"):
+    for name in ("ulysses", "unified", "ulysses_anything"):
         w, step, keep = ulysses_step(dev, name)
         for _ in range(3):
             step()
@@ -447,6 +478,8 @@ def run_ours(args):
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
             "timed_wall_s": t_wall,
+            "step_ms_percentiles": {f"p{q}": float(np.percentile(times, q))
+                                    for q in (1, 10, 50, 90, 99)},
         }
         if aux is not None:
             line["aux"] = aux

@@ -200,6 +200,68 @@ def ulysses_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, degree:
     return unified_attention(q, k, v, degree, 1, scale, stream, buffers)
 
 
+def ulysses_anything_permute(x: torch.Tensor, degree: int, direction: int,
+                             heads: Optional[int] = None, out: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Ulysses Anything regroup (cpattn_ulysses_anything_permute).
+    direction +1: [B,S,H,D] -> [G,B,S,ceil(H/G),D] (padding slots untouched);
+    direction -1: [G,B,S,ceil(H/G),D] -> [B,S,H,D], ``heads`` = H required
+    unless ``out`` is given."""
+    lib = _lib.load()
+    G = int(degree)
+    if out is None:
+        if direction == 1:
+            B, S, H, D = x.shape
+            out = torch.empty(G, B, S, -(-H // max(G, 1)), D, device=x.device, dtype=x.dtype)
+        else:
+            if heads is None:
+                raise ValueError("the inverse regroup needs heads (or out)")
+            _, B, S, _, D = x.shape
+            out = torch.empty(B, S, int(heads), D, device=x.device, dtype=x.dtype)
+    dx, dy = _desc(x), _desc(out)
+    check(lib.cpattn_ulysses_anything_permute(dx, G, int(direction), dy, _stream_handle(stream)),
+          "cpattn_ulysses_anything_permute")
+    return out
+
+
+def ulysses_anything_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, degree: int,
+                               scale: Optional[float] = None,
+                               stream: Optional[torch.cuda.Stream] = None,
+                               buffers: Optional[dict] = None,
+                               causal: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Ulysses Anything on one GPU (Diffusers "Context parallelism", "Ulysses
+    Anything Attention": no divisibility of H or S by G; ring_degree 1).
+    q, k, v [B,S,H,D]: regroup into G tensor_split head groups padded to
+    ceil(H/G) slots, attention of every group over its own heads (one launch,
+    padding slots skipped), inverse regroup.  Returns (out [B,S,H,D],
+    lse f32 [G,B,ceil(H/G),S] whose padding slots are unspecified)."""
+    lib = _lib.load()
+    B, S, H, D = q.shape
+    G = int(degree)
+    hm = -(-H // max(G, 1))
+    bufs = buffers if buffers is not None else {}
+
+    def buf(name, shape, dtype):
+        t = bufs.get(name)
+        if t is None or tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+            t = torch.empty(shape, device=q.device, dtype=dtype)
+            bufs[name] = t
+        return t
+
+    gshape = (G, B, S, hm, D)
+    qg = ulysses_anything_permute(q, G, 1, out=buf("q", gshape, q.dtype), stream=stream)
+    kg = ulysses_anything_permute(k, G, 1, out=buf("k", gshape, k.dtype), stream=stream)
+    vg = ulysses_anything_permute(v, G, 1, out=buf("v", gshape, v.dtype), stream=stream)
+    og = buf("o", gshape, q.dtype)
+    lse = buf("lse", (G, B, hm, S), torch.float32)
+    check(lib.cpattn_ulysses_anything_attention(_desc(qg), _desc(kg), _desc(vg), _scale(scale), H,
+                                                int(bool(causal)), _desc(og), _desc(lse),
+                                                _stream_handle(stream)),
+          "cpattn_ulysses_anything_attention")
+    out = ulysses_anything_permute(og, G, -1, out=buf("out", (B, S, H, D), q.dtype), stream=stream)
+    return out, lse
+
+
 def last_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronises the stream and returns (and clears) the device error word
     status: 0 = ok, 9 = a kernel-side wait timed out."""

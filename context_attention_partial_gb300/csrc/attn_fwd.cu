@@ -243,7 +243,7 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
   __syncwarp();
 }
 
-template <typename T, int D, bool CAUSAL>
+template <typename T, int D, bool CAUSAL, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -286,6 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       (kNT * kBM);
   const int h = CAUSAL ? blockIdx.x : blockIdx.y;
   const int b = CAUSAL ? blockIdx.y : blockIdx.z;
+  if constexpr (GROUPED) {
+    // Ulysses Anything: b = group * (batch / G) + batch index; head slots
+    // past the group's own heads are padding (uniform per CTA, before any
+    // barrier or TMEM allocation)
+    const int g = b / (p.batch / p.group_count);
+    const int hg = p.group_heads / p.group_count + (g < p.group_heads % p.group_count ? 1 : 0);
+    if (h >= hg) return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(BAR_Q, 1);
@@ -696,11 +704,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int D, bool CAUSAL>
+template <typename T, int D, bool CAUSAL, bool GROUPED>
 cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                         const AttnParams& p, cudaStream_t stream) {
   using C = Cfg<T, D>;
-  auto kernel = attn_fwd_kernel<T, D, CAUSAL>;
+  auto kernel = attn_fwd_kernel<T, D, CAUSAL, GROUPED>;
   // The setmaxnreg split assumes exactly kLaunchRegs registers per thread at
   // launch; with fewer, the softmax warpgroups' increase could never be
   // granted.  Refuse to launch such a build.
@@ -716,21 +724,30 @@ cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
   return cudaGetLastError();
 }
 
+// causal masking and the Ulysses Anything head skip are compiled in only
+// where a launch asks for them, so the plain kernel carries neither
+template <typename T, int D>
+cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                           const CUtensorMap& tm_v, const AttnParams& p, cudaStream_t stream) {
+  const bool grouped = p.group_count > 0;
+  if (p.causal != 0)
+    return grouped ? launch_impl<T, D, true, true>(tm_q, tm_k, tm_v, p, stream)
+                   : launch_impl<T, D, true, false>(tm_q, tm_k, tm_v, p, stream);
+  return grouped ? launch_impl<T, D, false, true>(tm_q, tm_k, tm_v, p, stream)
+                 : launch_impl<T, D, false, false>(tm_q, tm_k, tm_v, p, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_attention(InDtype dt, int head_dim, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const AttnParams& p, cudaStream_t stream) {
-  const bool c = p.causal != 0;
   if (dt == InDtype::BF16 && head_dim == 128)
-    return c ? launch_impl<__nv_bfloat16, 128, true>(tm_q, tm_k, tm_v, p, stream)
-             : launch_impl<__nv_bfloat16, 128, false>(tm_q, tm_k, tm_v, p, stream);
+    return launch_variant<__nv_bfloat16, 128>(tm_q, tm_k, tm_v, p, stream);
   if (dt == InDtype::BF16 && head_dim == 64)
-    return c ? launch_impl<__nv_bfloat16, 64, true>(tm_q, tm_k, tm_v, p, stream)
-             : launch_impl<__nv_bfloat16, 64, false>(tm_q, tm_k, tm_v, p, stream);
+    return launch_variant<__nv_bfloat16, 64>(tm_q, tm_k, tm_v, p, stream);
   if (dt == InDtype::F32 && head_dim == 64)
-    return c ? launch_impl<float, 64, true>(tm_q, tm_k, tm_v, p, stream)
-             : launch_impl<float, 64, false>(tm_q, tm_k, tm_v, p, stream);
+    return launch_variant<float, 64>(tm_q, tm_k, tm_v, p, stream);
   return cudaErrorInvalidValue;
 }
 

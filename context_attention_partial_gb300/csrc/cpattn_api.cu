@@ -150,7 +150,8 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
                             const cpattn_tensor* v, float scale, int ring_degree,
                             int ring_anything, cpattn_tensor* out, cpattn_tensor* lse,
                             void* workspace, size_t workspace_bytes, bool out_f32,
-                            bool causal, cudaStream_t stream) {
+                            bool causal, cudaStream_t stream, int group_count = 0,
+                            int group_heads = 0) {
   cpattn_status st = check_qkv(q, k, v);
   if (st != CPATTN_OK) return st;
   if (!out || !lse) return CPATTN_ERR_NULL;
@@ -217,6 +218,8 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   p.timeout_ns = g_timeout_ns.load();
   p.fault_skip_kv = g_fault_skip_kv.load();
   p.causal = causal ? 1 : 0;
+  p.group_count = group_count;
+  p.group_heads = group_heads;
   for (int c = 0; c <= ring_degree; ++c) p.chunk_start[c] = chunk_start[c];
   const cudaError_t e =
       cpattn::launch_attention(q->dtype == CPATTN_BF16 ? InDtype::BF16 : InDtype::F32,
@@ -338,6 +341,86 @@ cpattn_status cpattn_ulysses_permute(const cpattn_tensor* x, int degree, int dir
   p.elem_bytes = eb;
   const cudaError_t e = cpattn::launch_permute(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+cpattn_status cpattn_ulysses_anything_permute(const cpattn_tensor* x, int degree, int dir,
+                                              cpattn_tensor* y, void* stream) {
+  if (!x || !y) return CPATTN_ERR_NULL;
+  if (!dtype_known(x->dtype) || y->dtype != x->dtype) return CPATTN_ERR_DTYPE;
+  if (dir != 1 && dir != -1) return CPATTN_ERR_SHAPE;
+  if (degree < 1) return CPATTN_ERR_SHAPE;
+  const cpattn_tensor* flat = dir == 1 ? x : y;      // [B, S, H, D]
+  const cpattn_tensor* grouped = dir == 1 ? y : x;   // [G, B, S, ceil(H/G), D]
+  if (!shape_ok(flat, 4) || !shape_ok(grouped, 5)) return CPATTN_ERR_SHAPE;
+  const int64_t B = flat->shape[0], S = flat->shape[1], H = flat->shape[2], D = flat->shape[3];
+  const int64_t hm = (H + degree - 1) / degree;
+  if (grouped->shape[0] != degree || grouped->shape[1] != B || grouped->shape[2] != S ||
+      grouped->shape[3] != hm || grouped->shape[4] != D)
+    return CPATTN_ERR_SHAPE;
+  if (B * S * H * D == 0) return CPATTN_OK;
+  if (!x->data || !y->data) return CPATTN_ERR_NULL;
+  if (!contiguous(x) || !contiguous(y)) return CPATTN_ERR_LAYOUT;
+  const int eb = elem_bytes(x->dtype);
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x->data), ya = reinterpret_cast<uintptr_t>(y->data);
+  if (xa % eb || ya % eb) return CPATTN_ERR_LAYOUT;
+  const uintptr_t flat_bytes = static_cast<uintptr_t>(B * S * H * D * eb);
+  const uintptr_t grouped_bytes = static_cast<uintptr_t>(degree * B * S * hm * D * eb);
+  const uintptr_t xb = dir == 1 ? flat_bytes : grouped_bytes;
+  const uintptr_t yb = dir == 1 ? grouped_bytes : flat_bytes;
+  if (xa < ya + yb && ya < xa + xb) return CPATTN_ERR_LAYOUT;   // overlap
+  cpattn::PermuteParams p;
+  p.x = x->data;
+  p.y = y->data;
+  p.batch = B;
+  p.seq = S;
+  p.heads = H;
+  p.head_dim = D;
+  p.degree = degree;
+  p.dir = dir;
+  p.elem_bytes = eb;
+  const cudaError_t e = cpattn::launch_permute_anything(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+cpattn_status cpattn_ulysses_anything_attention(const cpattn_tensor* q, const cpattn_tensor* k,
+                                                const cpattn_tensor* v, float scale, int heads,
+                                                int is_causal, cpattn_tensor* out,
+                                                cpattn_tensor* lse, void* stream) {
+  if (!q || !k || !v || !out || !lse) return CPATTN_ERR_NULL;
+  const cpattn_tensor* five[4] = {q, k, v, out};
+  for (const cpattn_tensor* t : five)
+    if (!shape_ok(t, 5)) return CPATTN_ERR_SHAPE;
+  if (!shape_ok(lse, 4)) return CPATTN_ERR_SHAPE;
+  const int64_t G = q->shape[0], B = q->shape[1], S = q->shape[2], hm = q->shape[3];
+  if (heads < 1 || G < 1 || hm != (heads + G - 1) / G) return CPATTN_ERR_SHAPE;
+  for (const cpattn_tensor* t : five)
+    for (int i = 0; i < 5; ++i)
+      if (t->shape[i] != q->shape[i]) return CPATTN_ERR_SHAPE;
+  if (lse->shape[0] != G || lse->shape[1] != B || lse->shape[2] != hm || lse->shape[3] != S)
+    return CPATTN_ERR_SHAPE;
+  // the (group, batch) axes merge into one batch axis of the 4-D view
+  for (const cpattn_tensor* t : five)
+    if (G > 1 && B > 0 && t->stride[0] != B * t->stride[1]) return CPATTN_ERR_LAYOUT;
+  if (G > 1 && B > 0 && lse->stride[0] != B * lse->stride[1]) return CPATTN_ERR_LAYOUT;
+  if (G * B > 65535) return CPATTN_ERR_UNSUPPORTED;
+  // view [G*B, hm, S, D] (strides: batch, head, token, feature)
+  auto view = [&](const cpattn_tensor* t) {
+    cpattn_tensor w = *t;
+    w.ndim = 4;
+    w.shape[0] = G * B; w.shape[1] = hm; w.shape[2] = S; w.shape[3] = t->shape[4];
+    w.stride[0] = t->stride[1]; w.stride[1] = t->stride[3]; w.stride[2] = t->stride[2];
+    w.stride[3] = t->stride[4];
+    w.stride[4] = 0; w.shape[4] = 0;
+    return w;
+  };
+  cpattn_tensor vq = view(q), vk = view(k), vv = view(v), vo = view(out);
+  cpattn_tensor vl = *lse;
+  vl.ndim = 3;
+  vl.shape[0] = G * B; vl.shape[1] = hm; vl.shape[2] = S;
+  vl.stride[0] = lse->stride[1]; vl.stride[1] = lse->stride[2]; vl.stride[2] = lse->stride[3];
+  vl.shape[3] = vl.shape[4] = 0; vl.stride[3] = vl.stride[4] = 0;
+  return run_attention(&vq, &vk, &vv, scale, 1, 0, &vo, &vl, nullptr, 0, false, is_causal != 0,
+                       static_cast<cudaStream_t>(stream), static_cast<int>(G), heads);
 }
 
 const char* cpattn_status_string(cpattn_status status) {

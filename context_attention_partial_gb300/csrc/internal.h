@@ -25,6 +25,11 @@ struct AttnParams {
   unsigned long long timeout_ns;
   int fault_skip_kv;     // testing: the producer issues no K/V loads
   int causal;            // 1: query i attends keys j <= i (is_causal)
+  // Ulysses Anything: 0, or G when the batch axis is (group, batch) and the
+  // head axis holds ceil(H/G) slots of which group g fills its first h_g
+  // (tensor_split sizes of group_heads = H); padding slots are skipped
+  int group_count;
+  int group_heads;
   int chunk_start[CPATTN_MAX_RING_DEGREE + 1];
 };
 
@@ -56,6 +61,9 @@ struct PermuteParams {
   int elem_bytes;
 };
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream);
+// Ulysses Anything regroup between [B, S, H, D] and [G, B, S, ceil(H/G), D]
+// (heads = H; H need not divide by G).
+cudaError_t launch_permute_anything(const PermuteParams& p, cudaStream_t stream);
 
 // Error word helpers (defined with the device symbol).
 cudaError_t read_and_clear_device_error(unsigned int* value, cudaStream_t stream);

@@ -15,6 +15,10 @@
 //   contiguous on both sides; threads walk the destination in order with
 //   16-byte vectors (4 in flight per thread), or element by element when a
 //   segment is not a whole number of vectors.
+//   Ulysses Anything (Diffusers "Context parallelism", "Ulysses Anything
+//   Attention"): H need not divide by G; groups take tensor_split head counts
+//   and are padded to ceil(H/G) slots, which this copy neither writes nor
+//   reads.  The unit is one head row (16-byte vectors when D bytes allow).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -115,6 +119,55 @@ __global__ void __launch_bounds__(kPermuteThreads)
   }
 }
 
+// Ulysses Anything regroup.  Grid row blockIdx.y is one head h of the
+// [B, S, H, D] side; its group g and slot j follow from tensor_split (the
+// first r = H mod G groups hold q + 1 heads, the others q) once per block.
+// The block's threads then walk that head's B*S rows of `row` units
+// (16-byte vectors or elements): unit w of token tok sits at
+// (tok * H + h) * row + w on the flat side and at
+// ((g * bs + tok) * hm + j) * row + w on the grouped side, whose groups are
+// padded to hm = ceil(H/G) slots.
+template <typename V, typename Index, bool POW2>
+__global__ void __launch_bounds__(kPermuteThreads)
+    permute_anything_kernel(const V* __restrict__ x, V* __restrict__ y, Index per_head,
+                            Index row, int row_shift, Index heads, Index hm, Index bs, Index q,
+                            Index r, int dir) {
+  const Index h = blockIdx.y;
+  const Index big = r * (q + 1);
+  Index g, j;
+  if (h < big) {
+    g = h / (q + 1);
+    j = h - g * (q + 1);
+  } else {   // only reached when q > 0
+    g = r + (h - big) / q;
+    j = h - big - (g - r) * q;
+  }
+  const Index flat_base = h * row, flat_step = heads * row;
+  const Index grouped_base = (g * bs * hm + j) * row, grouped_step = hm * row;
+  const Index stride = static_cast<Index>(gridDim.x) * blockDim.x;
+  for (Index base = static_cast<Index>(blockIdx.x) * blockDim.x + threadIdx.x; base < per_head;
+       base += stride * kUnroll) {
+    V v[kUnroll];
+    Index src[kUnroll], dst[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const Index i = base + u * stride;
+      const Index tok = POW2 ? (i >> row_shift) : (i / row);
+      const Index w = i - tok * row;
+      const Index flat = flat_base + tok * flat_step + w;
+      const Index grouped = grouped_base + tok * grouped_step + w;
+      src[u] = dir > 0 ? flat : grouped;
+      dst[u] = dir > 0 ? grouped : flat;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (base + u * stride < per_head) v[u] = __ldcs(x + src[u]);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (base + u * stride < per_head) __stcs(y + dst[u], v[u]);
+  }
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -142,6 +195,53 @@ cudaError_t launch_permute_typed(const PermuteParams& p, int64_t total, int64_t 
   return cudaGetLastError();
 }
 
+template <typename V, typename Index>
+cudaError_t launch_permute_anything_index(const PermuteParams& p, int64_t per_head, int64_t row,
+                                          dim3 grid, cudaStream_t stream) {
+  const int64_t bs = p.batch * p.seq;
+  const int64_t hm = (p.heads + p.degree - 1) / p.degree;
+  const int64_t q = p.heads / p.degree, r = p.heads % p.degree;
+  int shift = 0;
+  while ((int64_t(1) << shift) < row) ++shift;
+  const V* x = static_cast<const V*>(p.x);
+  V* y = static_cast<V*>(p.y);
+  if ((int64_t(1) << shift) == row)
+    permute_anything_kernel<V, Index, true><<<grid, kPermuteThreads, 0, stream>>>(
+        x, y, static_cast<Index>(per_head), static_cast<Index>(row), shift,
+        static_cast<Index>(p.heads), static_cast<Index>(hm), static_cast<Index>(bs),
+        static_cast<Index>(q), static_cast<Index>(r), p.dir);
+  else
+    permute_anything_kernel<V, Index, false><<<grid, kPermuteThreads, 0, stream>>>(
+        x, y, static_cast<Index>(per_head), static_cast<Index>(row), shift,
+        static_cast<Index>(p.heads), static_cast<Index>(hm), static_cast<Index>(bs),
+        static_cast<Index>(q), static_cast<Index>(r), p.dir);
+  return cudaGetLastError();
+}
+
+template <typename V>
+cudaError_t launch_permute_anything_typed(const PermuteParams& p, int64_t row,
+                                          cudaStream_t stream) {
+  const int64_t bs = p.batch * p.seq;
+  const int64_t hm = (p.heads + p.degree - 1) / p.degree;
+  const int64_t per_head = bs * row;   // units of one head
+  // about 8 blocks of 256 threads per SM in total, spread over the heads
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  int64_t bx = (cap + p.heads - 1) / p.heads;
+  const int64_t want = (per_head + kPermuteThreads * kUnroll - 1) / (kPermuteThreads * kUnroll);
+  if (bx > want) bx = want;
+  if (bx < 1) bx = 1;
+  if (p.heads > 65535) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(p.heads));
+  // largest index on either side, and the loop counter's reach
+  const int64_t flat_total = bs * p.heads * row;
+  const int64_t grouped_total = p.degree * bs * hm * row;
+  const int64_t reach = per_head + bx * kPermuteThreads * kUnroll;
+  const int64_t lim = int64_t(1) << 31;
+  if (flat_total < lim && grouped_total < lim && reach < lim)
+    return launch_permute_anything_index<V, uint32_t>(p, per_head, row, grid, stream);
+  return launch_permute_anything_index<V, uint64_t>(p, per_head, row, grid, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
@@ -167,6 +267,18 @@ cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream) {
     return launch_permute_typed<unsigned short>(p, total_elems, seg_elems, stream);
   if (p.elem_bytes == 4)
     return launch_permute_typed<unsigned int>(p, total_elems, seg_elems, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_permute_anything(const PermuteParams& p, cudaStream_t stream) {
+  const int64_t total_elems = p.batch * p.seq * p.heads * p.head_dim;
+  if (total_elems == 0) return cudaSuccess;
+  const int64_t row_bytes = p.head_dim * p.elem_bytes;
+  const bool vec = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(p.x) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(p.y) % 16 == 0;
+  if (vec) return launch_permute_anything_typed<uint4>(p, row_bytes / 16, stream);
+  if (p.elem_bytes == 2) return launch_permute_anything_typed<unsigned short>(p, p.head_dim, stream);
+  if (p.elem_bytes == 4) return launch_permute_anything_typed<unsigned int>(p, p.head_dim, stream);
   return cudaErrorInvalidValue;
 }
 

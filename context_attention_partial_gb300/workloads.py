@@ -1,6 +1,6 @@
 """Seeded synthetic workloads.
 
-Shapes, dtypes and degrees of the five workloads, and the seeded generator of
+Shapes, dtypes and degrees of the workloads, and the seeded generator of
 their inputs.  This module holds none of the attention arithmetic: it is the
 one piece that both the CUDA path and the CPU oracle are fed from.
 
@@ -33,6 +33,7 @@ class Workload:
     layout: str = "bhsd"     # "bhsd": [B, H, S, D]; "bshd": [B, S, H, D]
     description: str = ""
     causal: bool = False     # query i attends keys j <= i
+    ulysses_anything: bool = False   # uneven head groups (tensor_split sizes)
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -75,6 +76,11 @@ WORKLOADS = {
                  layout="bshd",
                  description="Unified (Ulysses x Ring) on the FLUX-like shape: bf16 "
                              "[1,4608,24,128] (B,S,H,D), ulysses_degree 2, ring_degree 2"),
+        Workload("ulysses_anything", 1, 24, 4608, 128, "bf16", ulysses_degree=5,
+                 ulysses_anything=True, layout="bshd",
+                 description="Ulysses Anything on the FLUX-like shape: bf16 [1,4608,24,128] "
+                             "(B,S,H,D), ulysses_degree 5 (24 heads -> 5 5 5 5 4; "
+                             "4608 tokens not divisible by 5)"),
     ]
 }
 

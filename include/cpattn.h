@@ -1,12 +1,15 @@
 /*
  * cpattn.h -- C ABI of libcpattn.so: the data-parallel hot path of
- * context-parallel attention (Ring, Ring Anything and Ulysses) on one GB300.
+ * context-parallel attention (Ring, Ring Anything, Ulysses, Ulysses Anything
+ * and their Unified composition) on one GB300.
  *
  * Sources (page title, section):
  *   [CP]   Diffusers "Context parallelism" guide: variants table, "Ring
- *          Attention", "Ulysses Attention", "Ring Anything Attention".
+ *          Attention", "Ulysses Attention", "Unified Attention", "Ring
+ *          Anything Attention", "Ulysses Anything Attention".
  *   [API]  Diffusers "Parallelism" API page, ContextParallelConfig:
- *          ring_degree, ulysses_degree, convert_to_fp32, ring_anything.
+ *          ring_degree, ulysses_degree, convert_to_fp32, ring_anything,
+ *          ulysses_anything.
  *   [PARA] ParaAttention README, "Run Unified Attention ... with
  *          torch.compile": scaled_dot_product_attention with no mask, no
  *          dropout, not causal, on [B, H, S, D] tensors chunked on dim -2.
@@ -164,6 +167,49 @@ cpattn_status cpattn_ring_causal(const cpattn_tensor* q, const cpattn_tensor* k,
  */
 cpattn_status cpattn_ulysses_permute(const cpattn_tensor* x, int degree,
                                      int dir, cpattn_tensor* y, void* stream);
+
+/*
+ * cpattn_ulysses_anything_permute -- the head regroup of Ulysses Anything
+ * ([CP] "Ulysses Anything Attention", [API] ulysses_anything: Ulysses without
+ * the rule that H divides by G).  Heads are dealt out as torch.tensor_split
+ * does (G consecutive groups, the first H mod G of them one head longer);
+ * every group gets hm = ceil(H/G) head slots so the exchange buffer has one
+ * shape, and group g fills slots 0 .. h_g - 1:
+ *   dir = +1: x [B, S, H, D] -> y [G, B, S, hm, D],
+ *             y[g, b, s, j, :] = x[b, s, start_g + j, :] for j < h_g;
+ *             padding slots of y are not written.
+ *   dir = -1: x [G, B, S, hm, D] -> y [B, S, H, D] (the inverse map; padding
+ *             slots of x are not read).
+ * degree = G >= 1, any H >= 1 (groups past H hold no head).  Any dtype of
+ * this header.  x and y must be contiguous and must not overlap.  On one GPU
+ * every group keeps the whole sequence, so S needs no rule.
+ */
+cpattn_status cpattn_ulysses_anything_permute(const cpattn_tensor* x,
+                                              int degree, int dir,
+                                              cpattn_tensor* y, void* stream);
+
+/*
+ * cpattn_ulysses_anything_attention -- attention of every Ulysses Anything
+ * group over its own heads and the whole sequence, all groups in one launch
+ * ([CP] "Ulysses Anything Attention": ring_degree must be 1, so each group
+ * runs plain attention).
+ *   q, k, v, out [G, B, S, hm, D] in the layout cpattn_ulysses_anything_permute
+ *     writes (any strides with inner stride 1, 16-byte multiples elsewhere
+ *     and stride[0] = B * stride[1]); hm = ceil(heads / G).
+ *   heads = H, the total head count (it fixes each group's h_g).
+ *   is_causal: 0, or 1 for query i attending keys j <= i.
+ *   out: same dtype as q; lse [G, B, hm, S] f32 (stride[0] = B * stride[1]).
+ *   Padding slots j >= h_g of out and lse are not written.
+ * Dtypes and head sizes as cpattn_ring; G * B <= 65535.
+ */
+cpattn_status cpattn_ulysses_anything_attention(const cpattn_tensor* q,
+                                                const cpattn_tensor* k,
+                                                const cpattn_tensor* v,
+                                                float scale, int heads,
+                                                int is_causal,
+                                                cpattn_tensor* out,
+                                                cpattn_tensor* lse,
+                                                void* stream);
 
 /*
  * cpattn_ring_noalloc -- cpattn_ring for callers that cannot allocate device

@@ -122,6 +122,34 @@ def test_permute_validation():
                                       4, 1, y, None) == LAYOUT
 
 
+def test_ulysses_anything_validation():
+    lib = cp.load_library()
+    x = t((1, 16, 24, 128)); y = t((5, 1, 16, 5, 128), data=FAKE + (1 << 24))
+    perm = lib.cpattn_ulysses_anything_permute
+    assert perm(None, 5, 1, y, None) == NULL
+    assert perm(x, 0, 1, y, None) == SHAPE
+    assert perm(x, 5, 2, y, None) == SHAPE
+    assert perm(x, 5, 1, t((5, 1, 16, 4, 128), data=FAKE + (1 << 24)), None) == SHAPE  # not ceil(H/G)
+    assert perm(x, 5, 1, t((5, 1, 16, 5, 128), _lib.F32, data=FAKE + (1 << 24)), None) == DTYPE
+    assert perm(x, 5, 1, t((5, 1, 16, 5, 128), data=FAKE + 64), None) == LAYOUT        # overlap
+    assert perm(t((1, 16, 24, 128), stride=(16 * 24 * 256, 24 * 256, 256, 1)), 5, 1, y, None) == LAYOUT
+    z = t((1, 0, 24, 128), data=0)
+    assert perm(z, 5, 1, t((5, 1, 0, 5, 128), data=0), None) == OK
+    att = lib.cpattn_ulysses_anything_attention
+    g = t((5, 1, 256, 5, 128)); lse = t((5, 1, 5, 256), _lib.F32)
+    assert att(g, g, g, 0.0, 24, 0, g, None, None) == NULL
+    assert att(g, g, g, 0.0, 26, 0, g, lse, None) == SHAPE          # ceil(26/5) = 6 slots
+    assert att(g, g, g, 0.0, 0, 0, g, lse, None) == SHAPE
+    assert att(g, g, t((5, 1, 255, 5, 128)), 0.0, 24, 0, g, lse, None) == SHAPE
+    assert att(g, g, g, 0.0, 24, 0, g, t((5, 1, 256, 5), _lib.F32), None) == SHAPE
+    assert att(g, g, g, 0.0, 24, 0, t((5, 1, 256, 5, 128), _lib.F32), lse, None) == DTYPE
+    t96 = t((5, 1, 256, 5, 96))
+    assert att(t96, t96, t96, 0.0, 24, 0, t96, lse, None) == UNSUP
+    # the (group, batch) axes must merge into one batch axis
+    gb = t((5, 2, 256, 5, 128), stride=(4 * 256 * 5 * 128, 256 * 5 * 128, 5 * 128, 128, 1))
+    assert att(gb, gb, gb, 0.0, 24, 0, gb, t((5, 2, 5, 256), _lib.F32), None) == LAYOUT
+
+
 def test_python_binding_rejects_cpu_tensors():
     import torch
     q = torch.zeros(1, 1, 4, 64)

@@ -299,3 +299,84 @@ def test_unified_causal_matches_oracle():
     ro, rl = oracle.unified(q, k, v, 2, 3, 128 ** -0.5, causal=True)
     assert maxabs(out, ro) <= 1e-2
     assert maxabs(lse.reshape(2, 1, 4, 300), rl) <= 1e-3
+
+
+# ----------------------------------------------------------------------------
+# Ulysses Anything: uneven head groups padded to ceil(H/G) slots
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("shape,g,dtype", [
+    ((1, 4608, 24, 128), 5, torch.bfloat16),      # the Ulysses Anything workload's tensors
+    ((1, 4608, 24, 128), 7, torch.bfloat16),      # groups 4 4 4 3 3 3 3
+    ((2, 37, 7, 64), 3, torch.bfloat16),
+    ((1, 5, 6, 8), 4, torch.float32),             # groups 2 2 1 1
+    ((2, 3, 5, 3), 2, torch.bfloat16),            # 6-byte head rows: element path
+    ((1, 9, 2, 5), 4, torch.float32),             # H < G: two groups hold no head
+    ((2, 17, 8, 128), 4, torch.bfloat16),         # H % G == 0: plain Ulysses layout
+])
+def test_anything_permute_bit_exact(shape, g, dtype):
+    x = make_qkv(shape, dtype, seed=5)[0]
+    H = shape[2]
+    hm = -(-H // g)
+    sentinel = torch.full((g,) + shape[:2] + (hm, shape[3]), -3.0, dtype=dtype, device=DEV)
+    y = cp.ulysses_anything_permute(x.to(DEV), g, 1, out=sentinel)
+    torch.cuda.synchronize()
+    ref = oracle.ulysses_anything_permute(x, g, 1)
+    start = oracle.ulysses_anything_heads(H, g)
+    yc = y.cpu()
+    for gi in range(g):
+        hg = start[gi + 1] - start[gi]
+        assert torch.equal(yc[gi, :, :, :hg], ref[gi, :, :, :hg])
+        assert torch.all(yc[gi, :, :, hg:] == -3.0)            # padding not written
+    if H % g == 0:
+        assert torch.equal(yc, oracle.ulysses_permute(x, g, 1))
+    # the inverse does not read the padding: poison it first
+    for gi in range(g):
+        y[gi, :, :, start[gi + 1] - start[gi]:] = float("nan")
+    back = cp.ulysses_anything_permute(y, g, -1, heads=H)
+    torch.cuda.synchronize()
+    assert torch.equal(back.cpu(), x)
+
+
+@pytest.mark.parametrize("b,s,h,d,g,dt,causal", [
+    (1, 300, 5, 128, 2, torch.bfloat16, False),    # groups 3 2
+    (2, 257, 7, 64, 3, torch.bfloat16, False),     # groups 3 2 2
+    (1, 256, 5, 64, 3, torch.float32, False),      # fp32 (3xTF32)
+    (1, 200, 2, 128, 4, torch.bfloat16, False),    # H < G
+    (1, 300, 7, 128, 4, torch.bfloat16, True),     # causal, groups 2 2 2 1
+    (1, 130, 8, 128, 4, torch.bfloat16, False),    # even split
+])
+def test_ulysses_anything_matches_oracle(b, s, h, d, g, dt, causal):
+    q, k, v = make_qkv((b, s, h, d), dt, seed=47)
+    out, lse = cp.ulysses_anything_attention(q.to(DEV), k.to(DEV), v.to(DEV), g, causal=causal)
+    torch.cuda.synchronize()
+    status_ok()
+    ro, rl = oracle.ulysses_anything(q, k, v, g, d ** -0.5, causal=causal)
+    to, tl = TOL[dt]
+    assert out.shape == q.shape and out.dtype == dt
+    assert maxabs(out, ro) <= to
+    start = oracle.ulysses_anything_heads(h, g)
+    lc = lse.cpu().numpy()
+    for gi in range(g):
+        hg = start[gi + 1] - start[gi]
+        if hg:
+            assert float(np.max(np.abs(lc[gi, :, :hg] - rl[gi, :, :hg]))) <= tl
+
+
+def test_ulysses_anything_leaves_padding_slots_alone():
+    """The attention launch skips padding head slots: out and lse keep what
+    the caller put there."""
+    b, s, h, d, g = 1, 256, 5, 128, 3                     # groups 2 2 1, 2 slots
+    q, k, v = (x.to(DEV) for x in make_qkv((b, s, h, d), torch.bfloat16, seed=53))
+    qg, kg, vg = (cp.ulysses_anything_permute(x, g, 1) for x in (q, k, v))
+    og = torch.full_like(qg, 7.0)
+    lse = torch.full((g, b, 2, s), 9.0, device=DEV)
+    lib = cp.load_library()
+    from context_attention_partial_gb300 import api
+    rc = lib.cpattn_ulysses_anything_attention(api._desc(qg), api._desc(kg), api._desc(vg), 0.0, h,
+                                               0, api._desc(og), api._desc(lse),
+                                               torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    status_ok()
+    assert torch.all(og[2, :, :, 1] == 7.0) and torch.all(lse[2, :, 1] == 9.0)
+    assert torch.all(torch.isfinite(og[:2].float())) and not torch.any(lse[:2] == 9.0)

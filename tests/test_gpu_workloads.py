@@ -1,4 +1,4 @@
-"""The five workloads at full size, called exactly as bench.py calls them.
+"""The workloads at full size, called exactly as bench.py calls them.
 
 The oracle recomputes sampled query rows one by one (first and last rows,
 tile and chunk boundaries, the ragged tail, random rows, several heads and
@@ -130,6 +130,26 @@ def test_unified_sampled():
                              ring_degree=w.ring_degree)
         assert np.abs(out_c[0, rows, h].float().numpy() - ro[0]).max() <= 1e-2
         assert np.abs(lse_c[h // hg, h % hg, rows].numpy() - rl[0]).max() <= 1e-3
+
+
+def test_ulysses_anything_sampled():
+    """Ulysses Anything on the FLUX-like shape, 24 heads over 5 groups
+    (5 5 5 5 4): each head's rows equal attention over that head's full
+    sequence; heads on both sides of every group boundary are checked."""
+    w, q, k, v = make_workload("ulysses_anything", seed=0)   # [B, S, H, D]
+    out, lse = cp.ulysses_anything_attention(q.to(DEV), k.to(DEV), v.to(DEV), w.ulysses_degree)
+    torch.cuda.synchronize()
+    assert cp.last_device_status() == 0
+    check_convex(out, v.to(DEV), dims=1)
+    out_c, lse_c = out.cpu(), lse.cpu()
+    start = oracle.ulysses_anything_heads(w.heads, w.ulysses_degree)
+    for i, h in enumerate([0, 4, 5, 14, 15, 19, 20, 23]):
+        g = max(j for j in range(w.ulysses_degree) if start[j] <= h)
+        rows = sample_rows(w.seq, i, n_random=12)
+        ro, rl = oracle.attention(q[0, rows, h].unsqueeze(0), k[0, :, h].unsqueeze(0),
+                                  v[0, :, h].unsqueeze(0), w.head_dim ** -0.5)
+        assert np.abs(out_c[0, rows, h].float().numpy() - ro[0]).max() <= 1e-2, h
+        assert np.abs(lse_c[g, 0, h - start[g], rows].numpy() - rl[0]).max() <= 1e-3, h
 
 
 def test_workload_table_flops():
