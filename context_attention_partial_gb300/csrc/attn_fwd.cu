@@ -396,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kWarpMma) {
       // ---------------------------------------------------------- MMA issuer
-      // Descriptors are built once; each MMA only adds a compile-time
-      // constant (byte offset >> 4) to a base.
+      // Descriptors are built once; an MMA's operands are a base plus a
+      // compile-time offset (byte offset >> 4).
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(sKV, 16, 1024);
       const uint64_t v_desc = smem_desc_sw128(sKV, kBN * 128, 1024);
@@ -460,51 +460,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lk = 2 * j + 2, sk = lk % C::STAGES;
         const uint32_t phk = (lk / C::STAGES) & 1;
         const bool more = j + 1 < n_tiles;
-        uint64_t v_base;
-        // query tile 0: every wait of the group (P_0, V_j, K_{j+1}) comes
-        // before the first MMA, so the 16 MMAs go out back to back: the
-        // hardware MMA queue is only a few MMAs deep and drains during any
-        // wait placed between them.
-        ok = wait_all(bar_p(0), j & 1, kErrWaitMma);
-        if (!ok) break;
-        if constexpr (C::TF32) {
-          ok = wait_all(bar_vt_full(j & 1), (j >> 1) & 1, kErrWaitMma);
-          v_base = vt_desc + static_cast<uint64_t>(((j & 1) * C::VT_TILE_BYTES) >> 4);
-        } else {
+        if constexpr (!C::TF32) {
+          // Every wait that does not depend on the softmax comes first and
+          // all descriptors of both groups are built before P_0 is awaited,
+          // so that once it is seen only the MMAs are left to issue: this
+          // warp gets few issue slots beside the softmax warps of its SM
+          // sub-partition, and the hardware MMA queue is only a few MMAs
+          // deep, draining during any wait placed between MMAs.
           ok = wait_all(bar_full(sv), phv, kErrWaitMma);
-          v_base = v_desc + static_cast<uint64_t>((sv * C::KV_TILE_BYTES) >> 4);
-        }
-        if (ok && more) ok = wait_all(bar_full(sk), phk, kErrWaitMma);
-        if (C::TF32 && ok && more) ok = wait_all(BAR_KLO_FULL, (j + 1) & 1, kErrWaitMma);
-        if (!ok) break;
-        tc_fence_after();
-        if (leader) {
-          issue_pv(0, v_base, acc);
-          if (more) {
-            issue_qk(0, sk);
-            mma_commit(bar_s(0));
-          } else {
-            mma_commit(bar_o(0));
+          if (ok && more) ok = wait_all(bar_full(sk), phk, kErrWaitMma);
+          if (!ok) break;
+          // all descriptors share their high word; the low word holds the
+          // start address (no carry: shared memory is below 256 KB)
+          const uint32_t hi = static_cast<uint32_t>(q_desc >> 32);
+          const uint32_t vb = static_cast<uint32_t>(v_desc) + ((sv * C::KV_TILE_BYTES) >> 4);
+          const uint32_t kb = static_cast<uint32_t>(k_desc) + ((sk * C::KV_TILE_BYTES) >> 4);
+          uint32_t vd[C::PV_STEPS], kd[C::QK_STEPS], qd[C::QK_STEPS], pa[C::PV_STEPS];
+#pragma unroll
+          for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+            vd[kk] = vb + ((kk * C::KSTEP * 128) >> 4);
+            pa[kk] = tmem + kk * C::P_COLS_PER_STEP;
           }
-        }
-        __syncwarp();
-        // query tile 1
-        ok = wait_all(bar_p(1), j & 1, kErrWaitMma);
-        if (!ok) break;
-        tc_fence_after();
-        if (leader) {
-          issue_pv(1, v_base, acc);
-          if constexpr (C::TF32)
-            mma_commit(bar_vt_empty(j & 1));
-          else
+#pragma unroll
+          for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+            kd[kk] = kb + (((kk / 4) * (kBN * 128) + (kk % 4) * 32) >> 4);
+            qd[kk] = static_cast<uint32_t>(q_desc) + (((kk / 4) * (kBM * 128) + (kk % 4) * 32) >> 4);
+          }
+          ok = wait_all(bar_p(0), j & 1, kErrWaitMma);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) {
+            mma_group<C::PV_STEPS, false>(tmem + C::O_COL, pa, vd, hi, C::IDESC_PV, acc);
+            if (more) {
+              mma_group<C::QK_STEPS, true>(tmem, qd, kd, hi, C::IDESC_QK, 0u);
+              mma_commit(bar_s(0));
+            } else {
+              mma_commit(bar_o(0));
+            }
+          }
+          __syncwarp();
+          // query tile 1: P in the next S columns, Q in the next tile
+#pragma unroll
+          for (int kk = 0; kk < C::PV_STEPS; ++kk) pa[kk] += kBN;
+#pragma unroll
+          for (int kk = 0; kk < C::QK_STEPS; ++kk) qd[kk] += C::Q_TILE_BYTES >> 4;
+          ok = wait_all(bar_p(1), j & 1, kErrWaitMma);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) {
+            mma_group<C::PV_STEPS, false>(tmem + C::O_COL + D, pa, vd, hi, C::IDESC_PV, acc);
             mma_commit(bar_empty(sv));
-          if (more) {
-            issue_qk(1, sk);
-            mma_commit(bar_s(1));
-            mma_commit(bar_empty(sk));
-            if constexpr (C::TF32) mma_commit(BAR_KLO_EMPTY);
-          } else {
-            mma_commit(bar_o(1));
+            if (more) {
+              mma_group<C::QK_STEPS, true>(tmem + kBN, qd, kd, hi, C::IDESC_QK, 0u);
+              mma_commit(bar_s(1));
+              mma_commit(bar_empty(sk));
+            } else {
+              mma_commit(bar_o(1));
+            }
+          }
+        } else {
+          // fp32 inputs (3 MMAs per step): query tile 0, every wait of the
+          // group (P_0, transposed V_j, K_{j+1} and its low part) before the
+          // first MMA
+          ok = wait_all(bar_p(0), j & 1, kErrWaitMma);
+          if (!ok) break;
+          ok = wait_all(bar_vt_full(j & 1), (j >> 1) & 1, kErrWaitMma);
+          const uint64_t v_base = vt_desc + static_cast<uint64_t>(((j & 1) * C::VT_TILE_BYTES) >> 4);
+          if (ok && more) ok = wait_all(bar_full(sk), phk, kErrWaitMma);
+          if (ok && more) ok = wait_all(BAR_KLO_FULL, (j + 1) & 1, kErrWaitMma);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) {
+            issue_pv(0, v_base, acc);
+            if (more) {
+              issue_qk(0, sk);
+              mma_commit(bar_s(0));
+            } else {
+              mma_commit(bar_o(0));
+            }
+          }
+          __syncwarp();
+          // query tile 1
+          ok = wait_all(bar_p(1), j & 1, kErrWaitMma);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) {
+            issue_pv(1, v_base, acc);
+            mma_commit(bar_vt_empty(j & 1));
+            if (more) {
+              issue_qk(1, sk);
+              mma_commit(bar_s(1));
+              mma_commit(bar_empty(sk));
+              mma_commit(BAR_KLO_EMPTY);
+            } else {
+              mma_commit(bar_o(1));
+            }
           }
         }
         __syncwarp();

@@ -201,6 +201,114 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
   }
 }
 
+// N bf16 MMAs (kind::f16) from one asm statement: D (+)= A_i B_i, the first
+// accumulating into D iff acc != 0, the others always.  Operands are given
+// as the low 32-bit words of their shared-memory descriptors with one shared
+// high word (all descriptors here have equal strides, version and swizzle).
+// SS: A is a shared-memory descriptor; TS: A is a TMEM address.  One
+// statement keeps the issuing warp's instruction count per MMA minimal: that
+// warp shares its SM sub-partition with busy softmax warps and gets few
+// issue slots.
+template <int N, bool SS>
+__device__ __forceinline__ void mma_group(uint32_t d, const uint32_t* a, const uint32_t* b,
+                                          uint32_t hi, uint32_t idesc, uint32_t acc);
+template <>
+__device__ __forceinline__ void mma_group<4, true>(uint32_t d, const uint32_t* a, const uint32_t* b,
+                                                uint32_t hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"
+      "mov.b64 ra, {%1, %9};\n\t"
+      "mov.b64 rb, {%5, %9};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %11, p;\n\t"
+      "mov.b64 ra, {%2, %9};\n\t"
+      "mov.b64 rb, {%6, %9};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %11, t;\n\t"
+      "mov.b64 ra, {%3, %9};\n\t"
+      "mov.b64 rb, {%7, %9};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %11, t;\n\t"
+      "mov.b64 ra, {%4, %9};\n\t"
+      "mov.b64 rb, {%8, %9};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %11, t;\n\t"
+      "}\n" ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(hi), "r"(acc), "r"(idesc)
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void mma_group<4, false>(uint32_t d, const uint32_t* a, const uint32_t* b,
+                                                uint32_t hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"
+      "mov.b64 rb, {%5, %9};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], rb, %11, p;\n\t"
+      "mov.b64 rb, {%6, %9};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], rb, %11, t;\n\t"
+      "mov.b64 rb, {%7, %9};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], rb, %11, t;\n\t"
+      "mov.b64 rb, {%8, %9};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], rb, %11, t;\n\t"
+      "}\n" ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(hi), "r"(acc), "r"(idesc)
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void mma_group<8, true>(uint32_t d, const uint32_t* a, const uint32_t* b,
+                                                uint32_t hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p, %18, 0;\n\tsetp.eq.b32 t, %18, %18;\n\t"
+      "mov.b64 ra, {%1, %17};\n\t"
+      "mov.b64 rb, {%9, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %19, p;\n\t"
+      "mov.b64 ra, {%2, %17};\n\t"
+      "mov.b64 rb, {%10, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %19, t;\n\t"
+      "mov.b64 ra, {%3, %17};\n\t"
+      "mov.b64 rb, {%11, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %19, t;\n\t"
+      "mov.b64 ra, {%4, %17};\n\t"
+      "mov.b64 rb, {%12, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %19, t;\n\t"
+      "mov.b64 ra, {%5, %17};\n\t"
+      "mov.b64 rb, {%13, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %19, t;\n\t"
+      "mov.b64 ra, {%6, %17};\n\t"
+      "mov.b64 rb, {%14, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %19, t;\n\t"
+      "mov.b64 ra, {%7, %17};\n\t"
+      "mov.b64 rb, {%15, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %19, t;\n\t"
+      "mov.b64 ra, {%8, %17};\n\t"
+      "mov.b64 rb, {%16, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %19, t;\n\t"
+      "}\n" ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7]), "r"(hi), "r"(acc), "r"(idesc)
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void mma_group<8, false>(uint32_t d, const uint32_t* a, const uint32_t* b,
+                                                uint32_t hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p, %18, 0;\n\tsetp.eq.b32 t, %18, %18;\n\t"
+      "mov.b64 rb, {%9, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], rb, %19, p;\n\t"
+      "mov.b64 rb, {%10, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], rb, %19, t;\n\t"
+      "mov.b64 rb, {%11, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], rb, %19, t;\n\t"
+      "mov.b64 rb, {%12, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], rb, %19, t;\n\t"
+      "mov.b64 rb, {%13, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], rb, %19, t;\n\t"
+      "mov.b64 rb, {%14, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], rb, %19, t;\n\t"
+      "mov.b64 rb, {%15, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], rb, %19, t;\n\t"
+      "mov.b64 rb, {%16, %17};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], rb, %19, t;\n\t"
+      "}\n" ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7]), "r"(hi), "r"(acc), "r"(idesc)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
