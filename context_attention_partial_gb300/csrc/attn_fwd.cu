@@ -279,7 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // The warp index goes through a shuffle so that the compiler knows it is
+  // the same for every lane of a warp: each role's code is then uniform,
+  // which keeps the MMA warp's descriptors and loop state in uniform
+  // registers (FLUX ring 209 -> 195 us).
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x % 32;
   // causal: grid (H, B, query blocks), the heaviest query blocks first
   const int q_row0 =
       (CAUSAL ? static_cast<int>(gridDim.z - 1 - blockIdx.z) : static_cast<int>(blockIdx.x)) *
@@ -344,14 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 8) {
     regs_decrease<kControlRegs>();
     // The producer and MMA warps run their schedules with all 32 lanes, so
-    // every index, phase and descriptor stays warp-uniform; lane 0 alone
+    // every index, phase and descriptor stays warp-uniform; one elected lane
     // issues the TMA copies, the MMAs and the commits (a commit tracks the
     // MMAs of the thread that issues it).
     auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned code) {
       const bool r = mbar_wait(bar, parity, abort_flag, p.timeout_ns, &g_cpattn_device_error, code);
       return __all_sync(0xffffffffu, r);
     };
-    const bool leader = lane == 0;
+    const bool leader = elect_one();
     if (warp == kWarpProducer) {
       // ---------------------------------------------------------- producer
       if (leader) {

@@ -50,6 +50,15 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// One lane of the (fully active) warp, chosen by elect.sync: a leader the
+// compiler treats as a uniform choice.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t elected;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+               : "=r"(elected));
+  return elected != 0;
+}
+
 // Per-warpgroup register budget changes (all warps of a warpgroup execute
 // the same one).  The block's launch allocation must cover the new split.
 template <int N>
