@@ -480,6 +480,8 @@ def run_ours(args):
             "timed_wall_s": t_wall,
             "step_ms_percentiles": {f"p{q}": float(np.percentile(times, q))
                                     for q in (1, 10, 50, 90, 99)},
+            "step_ms_max": float(max(times)),
+            "steps_over_2x_median": int(sum(t > 2 * statistics.median(times) for t in times)),
         }
         if aux is not None:
             line["aux"] = aux
