@@ -674,29 +674,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.t == 0 && w.c > 0)
         chunk_epilogue<T, D>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok);
 
-      uint32_t s[kBN];
-      tmem_ld_x128(tS, s);
       // keys past the chunk's end, and with causal masking keys after this
       // row, are masked
       const int key0 = p.chunk_start[w.c] + w.t * kBN;
       int valid = p.chunk_start[w.c + 1] - key0;
       if constexpr (CAUSAL) valid = min(valid, q_row + 1 - key0);
-      if (CAUSAL ? __any_sync(0xffffffffu, valid < kBN) : valid < kBN) {
+      const bool masked = CAUSAL ? __any_sync(0xffffffffu, valid < kBN) : valid < kBN;
+      uint32_t s[kBN];
+      float row_max;
+      if (!masked) {
+        // the TMEM load returns the row max as well (no max pass)
+        tmem_ld_max_x128(tS, s, row_max);
+      } else {
+        tmem_ld_x128(tS, s);
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
           if (i >= valid) s[i] = f2u(-INFINITY);
-      }
-      float mx[4] = {u2f(s[0]), u2f(s[1]), u2f(s[2]), u2f(s[3])};
+        float mx[4] = {u2f(s[0]), u2f(s[1]), u2f(s[2]), u2f(s[3])};
 #pragma unroll
-      for (int i = 4; i < kBN; i += 8) {
-        mx[0] = fmax3(mx[0], u2f(s[i + 0]), u2f(s[i + 1]));
-        mx[1] = fmax3(mx[1], u2f(s[i + 2]), u2f(s[i + 3]));
-        if (i + 4 < kBN) {
-          mx[2] = fmax3(mx[2], u2f(s[i + 4]), u2f(s[i + 5]));
-          mx[3] = fmax3(mx[3], u2f(s[i + 6]), u2f(s[i + 7]));
+        for (int i = 4; i < kBN; i += 8) {
+          mx[0] = fmax3(mx[0], u2f(s[i + 0]), u2f(s[i + 1]));
+          mx[1] = fmax3(mx[1], u2f(s[i + 2]), u2f(s[i + 3]));
+          if (i + 4 < kBN) {
+            mx[2] = fmax3(mx[2], u2f(s[i + 4]), u2f(s[i + 5]));
+            mx[3] = fmax3(mx[3], u2f(s[i + 6]), u2f(s[i + 7]));
+          }
         }
+        row_max = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
       }
-      const float row_max = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
       const float m_tile = row_max * sl2;
       float factor = 1.f;
       bool need = false;
