@@ -373,30 +373,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = p.fault_skip_kv == 0;
       TileWalk w;
       w.start(p, kmax, r_eff);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int key0 = p.chunk_start[w.c] + w.t * kBN;
-        for (int which = 0; which < 2; ++which) {
-          const int s = ld % C::STAGES;
-          const uint32_t ph = (ld / C::STAGES) & 1;
-          ok = wait_all(bar_empty(s), ph ^ 1, kErrWaitProducer);
-          if (!ok) break;
-          if (leader) {
-            mbar_arrive_expect_tx(bar_full(s), C::KV_TILE_BYTES);
-            const CUtensorMap* tm = which == 0 ? &tm_k : &tm_v;
-            for (int kb = 0; kb < C::NKB; ++kb)
-              tma_load_4d(sKV + s * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar_full(s),
-                          kb * C::BOX_COLS, key0, h, b);
+      if constexpr (!C::TF32) {
+        // bf16: K_0 alone, then V_j and K_{j+1} as one pair on K_{j+1}'s
+        // full barrier (V_{n-1} alone on its own), so the MMA warp waits
+        // once per tile.  With an even stage count K always lands in an
+        // even stage and V in an odd one.
+        static_assert(C::STAGES % 2 == 0, "K/V pairing needs an even stage count");
+        auto load = [&](const CUtensorMap* tm, int stage, uint32_t bar, int key0) {
+          for (int kb = 0; kb < C::NKB; ++kb)
+            tma_load_4d(sKV + stage * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar,
+                        kb * C::BOX_COLS, key0, h, b);
+        };
+        if (ok) {
+          ok = wait_all(bar_empty(0), 1, kErrWaitProducer);
+          if (ok && leader) {
+            mbar_arrive_expect_tx(bar_full(0), C::KV_TILE_BYTES);
+            load(&tm_k, 0, bar_full(0), p.chunk_start[0]);
           }
           __syncwarp();
-          ++ld;
+          if (ok) ld = 1;
         }
-        w.next(p);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int key_v = p.chunk_start[w.c] + w.t * kBN;
+          w.next(p);
+          const bool more = j + 1 < n_tiles;
+          const int key_k = more ? p.chunk_start[w.c] + w.t * kBN : 0;
+          const int sv = ld % C::STAGES, sk = (ld + 1) % C::STAGES;
+          ok = wait_all(bar_empty(sv), ((ld / C::STAGES) & 1) ^ 1, kErrWaitProducer);
+          if (ok && more)
+            ok = wait_all(bar_empty(sk), (((ld + 1) / C::STAGES) & 1) ^ 1, kErrWaitProducer);
+          if (!ok) break;
+          if (leader) {
+            const uint32_t bar = more ? bar_full(sk) : bar_full(sv);
+            mbar_arrive_expect_tx(bar, (more ? 2 : 1) * C::KV_TILE_BYTES);
+            load(&tm_v, sv, bar, key_v);
+            if (more) load(&tm_k, sk, bar, key_k);
+          }
+          __syncwarp();
+          ld += more ? 2 : 1;
+        }
+      } else {
+        // fp32 inputs: K_j and V_j each on their own stage barrier
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int key0 = p.chunk_start[w.c] + w.t * kBN;
+          for (int which = 0; which < 2; ++which) {
+            const int s = ld % C::STAGES;
+            const uint32_t ph = (ld / C::STAGES) & 1;
+            ok = wait_all(bar_empty(s), ph ^ 1, kErrWaitProducer);
+            if (!ok) break;
+            if (leader) {
+              mbar_arrive_expect_tx(bar_full(s), C::KV_TILE_BYTES);
+              const CUtensorMap* tm = which == 0 ? &tm_k : &tm_v;
+              for (int kb = 0; kb < C::NKB; ++kb)
+                tma_load_4d(sKV + s * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar_full(s),
+                            kb * C::BOX_COLS, key0, h, b);
+            }
+            __syncwarp();
+            ++ld;
+          }
+          w.next(p);
+        }
       }
       if (!ok && leader) {
         // leave no copy in flight into this CTA's shared memory
         mbar_drain(BAR_Q, 0, p.timeout_ns);
-        for (int x = ld > C::STAGES ? ld - C::STAGES : 0; x < ld; ++x)
-          mbar_drain(bar_full(x % C::STAGES), (x / C::STAGES) & 1, p.timeout_ns);
+        for (int x = ld > C::STAGES ? ld - C::STAGES : 0; x < ld; ++x) {
+          if (C::TF32 || x % 2 == 0)
+            mbar_drain(bar_full(x % C::STAGES), (x / C::STAGES) & 1, p.timeout_ns);
+          else if (x + 1 >= ld)   // bf16: a V issued alone completes its own barrier once
+            mbar_drain(bar_full(x % C::STAGES), 0, p.timeout_ns);
+        }
       }
       __syncwarp();
     } else if (warp == kWarpMma) {
@@ -472,8 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // warp gets few issue slots beside the softmax warps of its SM
           // sub-partition, and the hardware MMA queue is only a few MMAs
           // deep, draining during any wait placed between MMAs.
-          ok = wait_all(bar_full(sv), phv, kErrWaitMma);
-          if (ok && more) ok = wait_all(bar_full(sk), phk, kErrWaitMma);
+          // V_j and K_{j+1} arrive together on K_{j+1}'s barrier; the last V
+          // alone completes its own barrier's first phase
+          ok = more ? wait_all(bar_full(sk), phk, kErrWaitMma) : wait_all(bar_full(sv), 0, kErrWaitMma);
           if (!ok) break;
           // all descriptors share their high word; the low word holds the
           // start address (no carry: shared memory is below 256 KB)
