@@ -520,8 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // deep, draining during any wait placed between MMAs.
           // V_j and K_{j+1} arrive together on K_{j+1}'s barrier; the last V
           // alone completes its own barrier's first phase
-          ok = more ? wait_all(bar_full(sk), phk, kErrWaitMma) : wait_all(bar_full(sv), 0, kErrWaitMma);
-          if (!ok) break;
+          const uint32_t kv_bar = more ? bar_full(sk) : bar_full(sv);
+          const uint32_t kv_ph = more ? phk : 0u;
+          // non-blocking probes first: their latency overlaps the descriptor
+          // build; a barrier found incomplete is waited for afterwards
+          const bool kv_now = mbar_test(kv_bar, kv_ph);
+          const bool p0_now = mbar_test(bar_p(0), j & 1);
           // all descriptors share their high word; the low word holds the
           // start address (no carry: shared memory is below 256 KB)
           const uint32_t hi = static_cast<uint32_t>(q_desc >> 32);
@@ -538,8 +542,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             kd[kk] = kb + (((kk / 4) * (kBN * 128) + (kk % 4) * 32) >> 4);
             qd[kk] = static_cast<uint32_t>(q_desc) + (((kk / 4) * (kBM * 128) + (kk % 4) * 32) >> 4);
           }
-          ok = wait_all(bar_p(0), j & 1, kErrWaitMma);
+          ok = __all_sync(0xffffffffu, kv_now) || wait_all(kv_bar, kv_ph, kErrWaitMma);
           if (!ok) break;
+          ok = __all_sync(0xffffffffu, p0_now) || wait_all(bar_p(0), j & 1, kErrWaitMma);
+          if (!ok) break;
+          // tile 1's P is probed now and waited for only if it was not yet
+          // complete (a completed phase cannot advance before this warp's
+          // next commit)
+          const bool p1_now = mbar_test(bar_p(1), j & 1);
           tc_fence_after();
           if (leader) {
             mma_group<C::PV_STEPS, false>(tmem + C::O_COL, pa, vd, hi, C::IDESC_PV, acc);
@@ -556,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < C::PV_STEPS; ++kk) pa[kk] += kBN;
 #pragma unroll
           for (int kk = 0; kk < C::QK_STEPS; ++kk) qd[kk] += C::Q_TILE_BYTES >> 4;
-          ok = wait_all(bar_p(1), j & 1, kErrWaitMma);
+          ok = __all_sync(0xffffffffu, p1_now) || wait_all(bar_p(1), j & 1, kErrWaitMma);
           if (!ok) break;
           tc_fence_after();
           if (leader) {
