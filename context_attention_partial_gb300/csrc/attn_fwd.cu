@@ -174,63 +174,68 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float factor) {
 template <typename T, int D>
 __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO, int c,
                                                int r_eff, float m_used, float l, int b, int h,
-                                               int q_row, bool row_ok) {
+                                               int q_row, bool row_ok, int64_t tile_id,
+                                               int tile_row) {
   const bool last = (c == r_eff - 1);
   // a row with no admissible key in the chunk (causal masking) emits the
   // empty partial (0, -inf): the identity of the merge below
   const bool empty = !(l > 0.f);
   const float inv_l = empty ? 0.f : 1.0f / l;
   const float lse_c = empty ? -INFINITY : (m_used + log2f(l)) * kLn2;
-  const int64_t flat = (static_cast<int64_t>(b) * p.heads + h) * p.s_q + q_row;
+  // running merged state per 128-row query tile, laid out [D/4][kBM][4]:
+  // the 32 lanes of a warp (32 consecutive rows) touch 512 contiguous bytes
+  // with each float4 access
+  float4* ws_tile = reinterpret_cast<float4*>(p.ws_o) + tile_id * (kBM * D / 4) + tile_row;
+  float* ws_lse = p.ws_lse + tile_id * kBM + tile_row;
   float w_run = 0.f, w_c = 1.f, lse_new = lse_c;
   if (c > 0 && row_ok) {
-    const float lse_run = p.ws_lse[flat];
+    const float lse_run = *ws_lse;
     const float hi = fmaxf(lse_run, lse_c), lo = fminf(lse_run, lse_c);
     lse_new = hi + log1pf(expf(lo - hi));
     w_run = expf(lse_run - lse_new);
     w_c = expf(lse_c - lse_new);
   }
-  float* ws_row = p.ws_o + flat * D;
+  constexpr int HC = D / 2;   // O columns per half
 #pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
-    uint32_t o[32];
+  for (int half = 0; half < 2; ++half) {
+    uint32_t o[HC];
     __syncwarp();
-    tmem_ld_x32(tO + c0, o);
+    if constexpr (HC == 64)
+      tmem_ld_x64(tO + half * HC, o);
+    else
+      tmem_ld_x32(tO + half * HC, o);
     if (row_ok) {
-      float v[32];
+      float4 v[HC / 4];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = u2f(o[i]) * inv_l;   // partial output o_c
+      for (int i = 0; i < HC / 4; ++i)   // partial output o_c
+        v[i] = make_float4(u2f(o[4 * i]) * inv_l, u2f(o[4 * i + 1]) * inv_l,
+                           u2f(o[4 * i + 2]) * inv_l, u2f(o[4 * i + 3]) * inv_l);
+      float4* slot = ws_tile + half * (HC / 4) * kBM;
       if (c > 0) {
-        const float4* src = reinterpret_cast<const float4*>(ws_row + c0);
+        float4 r[HC / 4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 r = src[i];
-          v[4 * i + 0] = w_run * r.x + w_c * v[4 * i + 0];
-          v[4 * i + 1] = w_run * r.y + w_c * v[4 * i + 1];
-          v[4 * i + 2] = w_run * r.z + w_c * v[4 * i + 2];
-          v[4 * i + 3] = w_run * r.w + w_c * v[4 * i + 3];
-        }
+        for (int i = 0; i < HC / 4; ++i) r[i] = slot[i * kBM];
+#pragma unroll
+        for (int i = 0; i < HC / 4; ++i)
+          v[i] = make_float4(w_run * r[i].x + w_c * v[i].x, w_run * r[i].y + w_c * v[i].y,
+                             w_run * r[i].z + w_c * v[i].z, w_run * r[i].w + w_c * v[i].w);
       }
       if (!last) {
-        float4* dst = reinterpret_cast<float4*>(ws_row + c0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < HC / 4; ++i) slot[i * kBM] = v[i];
       } else if (p.out_f32) {
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + b * p.out_sb +
-                                                h * p.out_sh + q_row * p.out_ss + c0);
+                                                h * p.out_sh + q_row * p.out_ss + half * HC);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < HC / 4; ++i) dst[i] = v[i];
       } else {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + b * p.out_sb +
-                                              h * p.out_sh + q_row * p.out_ss + c0);
+                                              h * p.out_sh + q_row * p.out_ss + half * HC);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]),
-                              pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                              pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
-                              pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        for (int i = 0; i < HC / 8; ++i)
+          dst[i] = make_uint4(pack_bf16x2(v[2 * i].x, v[2 * i].y), pack_bf16x2(v[2 * i].z, v[2 * i].w),
+                              pack_bf16x2(v[2 * i + 1].x, v[2 * i + 1].y),
+                              pack_bf16x2(v[2 * i + 1].z, v[2 * i + 1].w));
       }
     }
   }
@@ -238,7 +243,7 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
     if (last)
       p.lse[b * p.lse_sb + h * p.lse_sh + q_row * p.lse_ss] = lse_new;
     else
-      p.ws_lse[flat] = lse_new;
+      *ws_lse = lse_new;
   }
   __syncwarp();
 }
@@ -691,6 +696,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + wg * kBN;
     const uint32_t tO = tmem + lane_base + C::O_COL + wg * D;
     const int q_row = q_row0 + wg * kBM + quarter * 32 + lane;
+    // this row's query tile in the running-state workspace, and its row there
+    const int64_t tile_id = (static_cast<int64_t>(b) * p.heads + h) * ((p.s_q + kBM - 1) / kBM) +
+                            q_row0 / kBM + wg;
+    const int tile_row = quarter * 32 + lane;
     const bool row_ok = q_row < p.s_q;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
@@ -729,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (w.t == 0 && w.c > 0)
-        chunk_epilogue<T, D>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok);
+        chunk_epilogue<T, D>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok, tile_id, tile_row);
 
       // keys past the chunk's end, and with causal masking keys after this
       // row, are masked
@@ -808,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        chunk_epilogue<T, D>(p, tO, r_eff - 1, r_eff, m_used, l, b, h, q_row, row_ok);
+        chunk_epilogue<T, D>(p, tO, r_eff - 1, r_eff, m_used, l, b, h, q_row, row_ok, tile_id, tile_row);
       }
     }
   }

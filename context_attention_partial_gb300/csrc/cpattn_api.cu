@@ -128,7 +128,9 @@ cpattn_status ring_partition(int64_t s_kv, int ring_degree, int ring_anything, i
 
 size_t workspace_bytes_for(int64_t B, int64_t H, int64_t S, int64_t D, int ring_degree) {
   if (ring_degree <= 1) return 0;
-  return static_cast<size_t>(B * H * S) * static_cast<size_t>(D + 1) * sizeof(float);
+  // [B*H*ceil(S/128) query tiles][128 rows][D + 1] floats
+  const int64_t rows = B * H * ((S + 127) / 128) * 128;
+  return static_cast<size_t>(rows) * static_cast<size_t>(D + 1) * sizeof(float);
 }
 
 cpattn_status check_qkv(const cpattn_tensor* q, const cpattn_tensor* k, const cpattn_tensor* v) {
@@ -205,7 +207,7 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   p.lse_ss = lse->stride[2];
   if (need > 0) {
     p.ws_o = static_cast<float*>(workspace);
-    p.ws_lse = p.ws_o + B * H * S_q * D;
+    p.ws_lse = p.ws_o + B * H * ((S_q + 127) / 128) * 128 * D;
   }
   p.batch = static_cast<int>(B);
   p.heads = static_cast<int>(H);

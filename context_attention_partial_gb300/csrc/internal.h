@@ -16,8 +16,12 @@ struct AttnParams {
   int64_t out_sb, out_sh, out_ss;
   float* lse;            // [B, H, S_q] f32
   int64_t lse_sb, lse_sh, lse_ss;
-  float* ws_o;           // running merged output, f32 [B*H*S_q, D]  (ring_degree > 1)
-  float* ws_lse;         // running merged LSE, f32 [B*H*S_q]        (ring_degree > 1)
+  // running merged partial (ring_degree > 1), per 128-row query tile t of
+  // the B*H*ceil(S_q/128) tiles: ws_o f32 [t][D/4][128 rows][4] (a warp's
+  // float4 accesses at one column group are 512 contiguous bytes), ws_lse
+  // f32 [t][128 rows]
+  float* ws_o;
+  float* ws_lse;
   int batch, heads, s_q, s_kv;
   float scale_log2;      // softmax scale times log2(e)
   int ring_degree;

@@ -108,9 +108,11 @@ cpattn_status cpattn_merge(cpattn_tensor* out_a, cpattn_tensor* lse_a,
 
 /*
  * cpattn_ring_workspace_bytes -- bytes of device workspace cpattn_ring needs
- * for q [B, H, S_q, D] and this ring_degree: the running merged output
- * (f32 [B, H, S_q, D]) and its LSE (f32 [B, H, S_q]); 0 when ring_degree = 1.
- * Returns 0 for an invalid descriptor.
+ * for q [B, H, S_q, D] and this ring_degree: the running merged output and
+ * its LSE in f32, S_q rounded up to a multiple of 128 rows:
+ * B * H * ceil(S_q / 128) * 128 * (D + 1) * 4 bytes; 0 when ring_degree = 1.
+ * The layout inside is private to the library.  Returns 0 for an invalid
+ * descriptor.
  */
 size_t cpattn_ring_workspace_bytes(const cpattn_tensor* q, int ring_degree);
 
