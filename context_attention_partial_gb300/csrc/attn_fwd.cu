@@ -175,7 +175,7 @@ template <typename T, int D>
 __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO, int c,
                                                int r_eff, float m_used, float l, int b, int h,
                                                int q_row, bool row_ok, int64_t tile_id,
-                                               int tile_row) {
+                                               int tile_row, uint8_t* stage) {
   const bool last = (c == r_eff - 1);
   // a row with no admissible key in the chunk (causal masking) emits the
   // empty partial (0, -inf): the identity of the merge below
@@ -196,6 +196,11 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
     w_c = expf(lse_c - lse_new);
   }
   constexpr int HC = D / 2;   // O columns per half
+  const int lane = tile_row % 32;
+  // the final output goes through the warp's staging area when its element
+  // has the input's size (bf16 -> bf16, f32 -> f32): 16-byte chunks per row
+  const bool staged = (p.out_f32 != 0) == (sizeof(T) == 4);
+  constexpr int kCPR = D * static_cast<int>(sizeof(T)) / 16;
 #pragma unroll 1
   for (int half = 0; half < 2; ++half) {
     uint32_t o[HC];
@@ -223,19 +228,48 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
       if (!last) {
 #pragma unroll
         for (int i = 0; i < HC / 4; ++i) slot[i * kBM] = v[i];
-      } else if (p.out_f32) {
+      } else if (!staged) {
+        // f32 output of bf16 inputs (a single partial): straight to memory
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + b * p.out_sb +
                                                 h * p.out_sh + q_row * p.out_ss + half * HC);
 #pragma unroll
         for (int i = 0; i < HC / 4; ++i) dst[i] = v[i];
       } else {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + b * p.out_sb +
-                                              h * p.out_sh + q_row * p.out_ss + half * HC);
+        // final output: this lane's row into the warp's staging area
+        // (16-byte chunks XOR-swizzled by row against bank conflicts)
+        uint4* srow = reinterpret_cast<uint4*>(stage) + lane * kCPR;
+        if constexpr (sizeof(T) == 4) {
 #pragma unroll
-        for (int i = 0; i < HC / 8; ++i)
-          dst[i] = make_uint4(pack_bf16x2(v[2 * i].x, v[2 * i].y), pack_bf16x2(v[2 * i].z, v[2 * i].w),
-                              pack_bf16x2(v[2 * i + 1].x, v[2 * i + 1].y),
-                              pack_bf16x2(v[2 * i + 1].z, v[2 * i + 1].w));
+          for (int i = 0; i < HC / 4; ++i) {
+            const int c = half * (HC / 4) + i;
+            srow[c ^ (lane % kCPR)] = make_uint4(f2u(v[i].x), f2u(v[i].y), f2u(v[i].z), f2u(v[i].w));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < HC / 8; ++i) {
+            const int c = half * (HC / 8) + i;
+            srow[c ^ (lane % kCPR)] =
+                make_uint4(pack_bf16x2(v[2 * i].x, v[2 * i].y), pack_bf16x2(v[2 * i].z, v[2 * i].w),
+                           pack_bf16x2(v[2 * i + 1].x, v[2 * i + 1].y),
+                           pack_bf16x2(v[2 * i + 1].z, v[2 * i + 1].w));
+          }
+        }
+      }
+    }
+  }
+  if (last && staged) {
+    // the warp's 32 rows leave the staging area as whole rows: half a warp
+    // writes one row's bytes contiguously
+    __syncwarp();
+    const int row0 = q_row - lane;
+    constexpr int64_t es = sizeof(T);
+    uint8_t* out_base = static_cast<uint8_t*>(p.out) + (b * p.out_sb + h * p.out_sh) * es;
+#pragma unroll
+    for (int it = 0; it < kCPR; ++it) {
+      const int idx = it * 32 + lane, r = idx / kCPR, c = idx % kCPR;
+      if (row0 + r < p.s_q) {
+        const uint4 val = reinterpret_cast<const uint4*>(stage)[r * kCPR + (c ^ (r % kCPR))];
+        *reinterpret_cast<uint4*>(out_base + (row0 + r) * p.out_ss * es + c * 16) = val;
       }
     }
   }
@@ -738,7 +772,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (w.t == 0 && w.c > 0)
-        chunk_epilogue<T, D>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok, tile_id, tile_row);
+        chunk_epilogue<T, D>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok, tile_id, tile_row,
+                             nullptr);
 
       // keys past the chunk's end, and with causal masking keys after this
       // row, are masked
@@ -817,7 +852,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        chunk_epilogue<T, D>(p, tO, r_eff - 1, r_eff, m_used, l, b, h, q_row, row_ok, tile_id, tile_row);
+        // the Q tiles are idle once every Q K has completed: each warp
+        // stages its 32 output rows there (32 x D x out bytes = 8 KB)
+        chunk_epilogue<T, D>(p, tO, r_eff - 1, r_eff, m_used, l, b, h, q_row, row_ok, tile_id, tile_row,
+                             smem + warp * 32 * D * sizeof(T));
       }
     }
   }
