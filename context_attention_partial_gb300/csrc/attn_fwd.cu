@@ -363,6 +363,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *abort_flag = 0;
     fence_mbar_init();
+    // The Q tiles (and, bf16, the first K tile) are requested before the
+    // block-wide barrier, so their latency overlaps the rest of the setup.
+    mbar_arrive_expect_tx(BAR_Q, kNT * C::Q_TILE_BYTES);
+    for (int i = 0; i < kNT; ++i)
+      for (int kb = 0; kb < C::NKB; ++kb)
+        tma_load_4d(sQ + i * C::Q_TILE_BYTES + kb * kBM * 128, &tm_q, BAR_Q, kb * C::BOX_COLS,
+                    q_row0 + i * kBM, h, b);
+    if (!C::TF32 && p.fault_skip_kv == 0) {
+      mbar_arrive_expect_tx(bar_full(0), C::KV_TILE_BYTES);
+      for (int kb = 0; kb < C::NKB; ++kb)
+        tma_load_4d(sKV + kb * kBN * 128, &tm_k, bar_full(0), kb * C::BOX_COLS, p.chunk_start[0], h,
+                    b);
+    }
   }
   if (warp == kWarpMma) tmem_alloc(smem_addr(tmem_holder), kTmemCols);
   if (warp == kWarpProducer && lane == 0) {
@@ -380,10 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (INT_MAX - 1 without causal masking, so that kmax + 1 cannot overflow)
   const int kmax = CAUSAL ? min(q_row0 + kNT * kBM, p.s_q) - 1 : 0x7ffffffe;
   int r_eff = p.ring_degree;
-  if (CAUSAL)
+  int n_tiles = p.n_tiles_all;   // (computed by the host without causal masking)
+  if (CAUSAL) {
     while (r_eff > 1 && p.chunk_start[r_eff - 1] > kmax) --r_eff;
-  int n_tiles = 0;
-  for (int c = 0; c < r_eff; ++c) n_tiles += chunk_tiles(p, c, kmax);
+    n_tiles = 0;
+    for (int c = 0; c < r_eff; ++c) n_tiles += chunk_tiles(p, c, kmax);
+  }
 
   if (warp >= 8) {
     regs_decrease<kControlRegs>();
@@ -398,14 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = elect_one();
     if (warp == kWarpProducer) {
       // ---------------------------------------------------------- producer
-      if (leader) {
-        mbar_arrive_expect_tx(BAR_Q, kNT * C::Q_TILE_BYTES);
-        for (int i = 0; i < kNT; ++i)
-          for (int kb = 0; kb < C::NKB; ++kb)
-            tma_load_4d(sQ + i * C::Q_TILE_BYTES + kb * kBM * 128, &tm_q, BAR_Q,
-                        kb * C::BOX_COLS, q_row0 + i * kBM, h, b);
-      }
-      __syncwarp();
+      // (the Q tiles and bf16's K_0 were requested during the setup)
       int ld = 0;
       // fault injection (testing): no K/V copies, so every consumer's
       // bounded wait runs out and the CTA takes the abort path
@@ -423,15 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(sKV + stage * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar,
                         kb * C::BOX_COLS, key0, h, b);
         };
-        if (ok) {
-          ok = wait_all(bar_empty(0), 1, kErrWaitProducer);
-          if (ok && leader) {
-            mbar_arrive_expect_tx(bar_full(0), C::KV_TILE_BYTES);
-            load(&tm_k, 0, bar_full(0), p.chunk_start[0]);
-          }
-          __syncwarp();
-          if (ok) ld = 1;
-        }
+        if (ok) ld = 1;   // K_0
         for (int j = 0; j < n_tiles && ok; ++j) {
           const int key_v = p.chunk_start[w.c] + w.t * kBN;
           w.next(p);

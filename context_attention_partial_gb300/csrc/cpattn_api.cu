@@ -223,6 +223,8 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   p.group_count = group_count;
   p.group_heads = group_heads;
   for (int c = 0; c <= ring_degree; ++c) p.chunk_start[c] = chunk_start[c];
+  p.n_tiles_all = 0;
+  for (int c = 0; c < ring_degree; ++c) p.n_tiles_all += (chunk_start[c + 1] - chunk_start[c] + 127) / 128;
   const cudaError_t e =
       cpattn::launch_attention(q->dtype == CPATTN_BF16 ? InDtype::BF16 : InDtype::F32,
                                static_cast<int>(D), tm_q, tm_k, tm_v, p, stream);

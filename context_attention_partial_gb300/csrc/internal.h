@@ -34,6 +34,7 @@ struct AttnParams {
   // (tensor_split sizes of group_heads = H); padding slots are skipped
   int group_count;
   int group_heads;
+  int n_tiles_all;       // key tiles over all chunks (the count without causal masking)
   int chunk_start[CPATTN_MAX_RING_DEGREE + 1];
 };
 
