@@ -26,6 +26,10 @@
 //               -> row sum, P (bf16, or fp32 for tf32) back into S's columns;
 //               at each chunk end the normalised partial is merged in fp32
 //               with the running result (held in a global fp32 workspace).
+//   Without causal masking (bf16), once every K/V tile is in flight the
+//   producer also bulk-copies the running result that the final merge
+//   reads into shared memory (a spare region plus three released stages),
+//   so the last epilogue reads it there instead of from global memory.
 //   setmaxnreg moves registers from the control warpgroup (warps 8-11) to
 //   the two softmax warpgroups.
 //   TMEM (512 columns): S_0 | S_1 | O_0 | O_1.
@@ -89,9 +93,18 @@ struct Cfg {
   static constexpr int STAGES_FIT =
       (SMEM_BUDGET - kNT * Q_TILE_BYTES - VT_BUFS * VT_TILE_BYTES - KLO_BYTES) / KV_TILE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int NUM_BARS = 1 + 2 * STAGES + 3 * kNT + 1 + 2 * VT_BUFS + (TF32 ? 3 : 0);
+  // bf16 without causal masking: the final merge's running state (fp32,
+  // kNT query tiles x D) is fetched into shared memory as 2 kNT pieces of
+  // one K/V tile's size each (half of D of one query tile): one into a
+  // region of its own, the others into the stages released first once
+  // every K/V tile is in flight
+  static constexpr int WS_PIECE_BYTES = kBM * (D / 2) * 4;
+  static constexpr int WSX_BYTES = TF32 ? 0 : WS_PIECE_BYTES;
+  static constexpr int NUM_BARS =
+      1 + 2 * STAGES + 3 * kNT + 1 + 2 * VT_BUFS + (TF32 ? 3 : 0) + 2 * kNT;
   static constexpr int SMEM_BYTES = 1024 + kNT * Q_TILE_BYTES + STAGES * KV_TILE_BYTES +
-                                    VT_BUFS * VT_TILE_BYTES + KLO_BYTES + NUM_BARS * 8 + 16;
+                                    VT_BUFS * VT_TILE_BYTES + KLO_BYTES + WSX_BYTES +
+                                    NUM_BARS * 8 + 16;
   static constexpr int KSTEP = 32 / ES;             // K elements per MMA (32 bytes)
   static constexpr int QK_STEPS = ROW_BYTES / 32;
   static constexpr int PV_STEPS = kBN / KSTEP;
@@ -106,6 +119,8 @@ struct Cfg {
   static_assert(!TF32 || (D == 64 && QLO_COL + kNT * D <= (int)kTmemCols), "tf32 TMEM budget");
   static_assert(!TF32 || STAGES % 2 == 0, "fp32 inputs keep K tiles on even stages");
   static_assert(STAGES >= 2, "need at least two K/V stages");
+  static_assert(TF32 || (WS_PIECE_BYTES == KV_TILE_BYTES && STAGES >= 2 * kNT),
+                "running-state pieces reuse K/V stages");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -171,11 +186,15 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float factor) {
 
 // End of chunk c for this thread's query row: emit the chunk's partial
 // (o_c = O / l, lse_c = m ln2 + ln l) and fold it into the running result.
-template <typename T, int D>
+// PRE: the running state was prefetched into shared memory (pre0, pre1:
+// byte offsets from sbase of the pieces holding D's first and second half,
+// in the workspace tile's layout).
+template <typename T, int D, bool PRE>
 __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO, int c,
                                                int r_eff, float m_used, float l, int b, int h,
                                                int q_row, bool row_ok, int64_t tile_id,
-                                               int tile_row, uint8_t* stage) {
+                                               int tile_row, uint8_t* stage, float lse_run,
+                                               const uint8_t* sbase, uint32_t pre0, uint32_t pre1) {
   const bool last = (c == r_eff - 1);
   // a row with no admissible key in the chunk (causal masking) emits the
   // empty partial (0, -inf): the identity of the merge below
@@ -189,41 +208,59 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
   float* ws_lse = p.ws_lse + tile_id * kBM + tile_row;
   float w_run = 0.f, w_c = 1.f, lse_new = lse_c;
   if (c > 0 && row_ok) {
-    const float lse_run = *ws_lse;
     const float hi = fmaxf(lse_run, lse_c), lo = fminf(lse_run, lse_c);
     lse_new = hi + log1pf(expf(lo - hi));
     w_run = expf(lse_run - lse_new);
     w_c = expf(lse_c - lse_new);
   }
-  constexpr int HC = D / 2;   // O columns per half
+  // O columns per part: halves, or quarters when the running state comes
+  // from shared memory (it is read in the same pass, so the part is smaller)
+  constexpr int NPARTS = PRE ? 4 : 2;
+  constexpr int HC = D / NPARTS;
   const int lane = tile_row % 32;
   // the final output goes through the warp's staging area when its element
   // has the input's size (bf16 -> bf16, f32 -> f32): 16-byte chunks per row
   const bool staged = (p.out_f32 != 0) == (sizeof(T) == 4);
   constexpr int kCPR = D * static_cast<int>(sizeof(T)) / 16;
 #pragma unroll 1
-  for (int half = 0; half < 2; ++half) {
+  for (int part = 0; part < NPARTS; ++part) {
     uint32_t o[HC];
     __syncwarp();
     if constexpr (HC == 64)
-      tmem_ld_x64(tO + half * HC, o);
+      tmem_ld_x64(tO + part * HC, o);
+    else if constexpr (HC == 32)
+      tmem_ld_x32(tO + part * HC, o);
     else
-      tmem_ld_x32(tO + half * HC, o);
+      tmem_ld_x16(tO + part * HC, o);
     if (row_ok) {
       float4 v[HC / 4];
 #pragma unroll
       for (int i = 0; i < HC / 4; ++i)   // partial output o_c
         v[i] = make_float4(u2f(o[4 * i]) * inv_l, u2f(o[4 * i + 1]) * inv_l,
                            u2f(o[4 * i + 2]) * inv_l, u2f(o[4 * i + 3]) * inv_l);
-      float4* slot = ws_tile + half * (HC / 4) * kBM;
+      float4* slot = ws_tile + part * (HC / 4) * kBM;
       if (c > 0) {
-        float4 r[HC / 4];
+        // the running state: prefetched into shared memory (same layout as
+        // the workspace tile, one piece per half of D) or read from the workspace
+        auto fold = [&](int i, const float4& r) {
+          v[i] = make_float4(w_run * r.x + w_c * v[i].x, w_run * r.y + w_c * v[i].y,
+                             w_run * r.z + w_c * v[i].z, w_run * r.w + w_c * v[i].w);
+        };
+        if constexpr (PRE) {
+          // shared-memory latency is short: each value is folded as it arrives
+          constexpr int kPerPiece = NPARTS / 2;
+          const float4* src =
+              reinterpret_cast<const float4*>(sbase + (part < kPerPiece ? pre0 : pre1)) +
+              (part % kPerPiece) * (HC / 4) * kBM + tile_row;
 #pragma unroll
-        for (int i = 0; i < HC / 4; ++i) r[i] = slot[i * kBM];
+          for (int i = 0; i < HC / 4; ++i) fold(i, src[i * kBM]);
+        } else {
+          float4 r[HC / 4];
 #pragma unroll
-        for (int i = 0; i < HC / 4; ++i)
-          v[i] = make_float4(w_run * r[i].x + w_c * v[i].x, w_run * r[i].y + w_c * v[i].y,
-                             w_run * r[i].z + w_c * v[i].z, w_run * r[i].w + w_c * v[i].w);
+          for (int i = 0; i < HC / 4; ++i) r[i] = slot[i * kBM];
+#pragma unroll
+          for (int i = 0; i < HC / 4; ++i) fold(i, r[i]);
+        }
       }
       if (!last) {
 #pragma unroll
@@ -231,7 +268,7 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
       } else if (!staged) {
         // f32 output of bf16 inputs (a single partial): straight to memory
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + b * p.out_sb +
-                                                h * p.out_sh + q_row * p.out_ss + half * HC);
+                                                h * p.out_sh + q_row * p.out_ss + part * HC);
 #pragma unroll
         for (int i = 0; i < HC / 4; ++i) dst[i] = v[i];
       } else {
@@ -241,13 +278,13 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
         if constexpr (sizeof(T) == 4) {
 #pragma unroll
           for (int i = 0; i < HC / 4; ++i) {
-            const int c = half * (HC / 4) + i;
+            const int c = part * (HC / 4) + i;
             srow[c ^ (lane % kCPR)] = make_uint4(f2u(v[i].x), f2u(v[i].y), f2u(v[i].z), f2u(v[i].w));
           }
         } else {
 #pragma unroll
           for (int i = 0; i < HC / 8; ++i) {
-            const int c = half * (HC / 8) + i;
+            const int c = part * (HC / 8) + i;
             srow[c ^ (lane % kCPR)] =
                 make_uint4(pack_bf16x2(v[2 * i].x, v[2 * i].y), pack_bf16x2(v[2 * i].z, v[2 * i].w),
                            pack_bf16x2(v[2 * i + 1].x, v[2 * i + 1].y),
@@ -289,6 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ AttnParams p) {
   using C = Cfg<T, D>;
+  // bf16 without causal masking prefetches the final merge's running state
+  // (the causal kernel has no registers to spare for it)
+  constexpr bool kPrefetchState = !C::TF32 && !CAUSAL;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -297,9 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sKV = sQ + kNT * C::Q_TILE_BYTES;
   const uint32_t sVt = sKV + C::STAGES * C::KV_TILE_BYTES;
   const uint32_t sKlo = sVt + C::VT_BUFS * C::VT_TILE_BYTES;
+  const uint32_t sWsx = sKlo + C::KLO_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kNT * C::Q_TILE_BYTES +
                                                C::STAGES * C::KV_TILE_BYTES +
-                                               C::VT_BUFS * C::VT_TILE_BYTES + C::KLO_BYTES);
+                                               C::VT_BUFS * C::VT_TILE_BYTES + C::KLO_BYTES +
+                                               C::WSX_BYTES);
   const uint32_t bar0 = smem_addr(bars);
   const uint32_t BAR_Q = bar0;
   auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
@@ -315,6 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t BAR_QLO = bar0 + 8u * (2 + 2 * C::STAGES + 3 * kNT + 2 * C::VT_BUFS);
   const uint32_t BAR_KLO_FULL = BAR_QLO + 8u;
   const uint32_t BAR_KLO_EMPTY = BAR_QLO + 16u;
+  auto bar_ws = [&](int i) { return bar0 + 8u * (C::NUM_BARS - 2 * kNT + i); };
+  // the running state of query tile i is written and fenced for the bulk copy
+  auto bar_ws_ready = [&](int i) { return bar0 + 8u * (C::NUM_BARS - kNT + i); };
+  // home of piece k of the final merge's running state (query tile k / 2,
+  // half k % 2 of D) with n key tiles: the spare region, then the stages of
+  // K/V loads 2n, 2n + 1, ..., whose previous tiles are released first
+  // (as a byte offset from the Q tiles' start)
+  auto ws_piece = [&](int k, int n) -> uint32_t {
+    return k == 0 ? sWsx - sQ : sKV - sQ + ((2 * n + k - 1) % C::STAGES) * C::KV_TILE_BYTES;
+  };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -352,6 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_o(i), 1);
     }
     mbar_init(BAR_DRAIN, 1);
+    for (int i = 0; i < kNT; ++i) {
+      mbar_init(bar_ws(i), 1);
+      mbar_init(bar_ws_ready(i), 4);   // one arrival per softmax warp
+    }
     for (int i = 0; i < C::VT_BUFS; ++i) {
       mbar_init(bar_vt_full(i), 1);
       mbar_init(bar_vt_empty(i), 1);
@@ -415,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- producer
       // (the Q tiles and bf16's K_0 were requested during the setup)
       int ld = 0;
+      int ws_armed = 0;   // query tiles whose running-state pieces are in flight
       // fault injection (testing): no K/V copies, so every consumer's
       // bounded wait runs out and the CTA takes the abort path
       bool ok = p.fault_skip_kv == 0;
@@ -451,6 +508,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           ld += more ? 2 : 1;
         }
+        // the final merge's running state, once every K/V tile is in flight:
+        // a query tile's two pieces are armed and issued together once both
+        // of their homes are free, so an abort never leaves one half-armed
+        if (kPrefetchState && ok && r_eff > 1) {
+          const int64_t tile0 =
+              (static_cast<int64_t>(b) * p.heads + h) * ((p.s_q + kBM - 1) / kBM) + q_row0 / kBM;
+          for (int i = 0; i < kNT && ok; ++i) {
+            if (q_row0 + i * kBM >= p.s_q) break;   // no such query tile, no state
+            ok = wait_all(bar_ws_ready(i), 0, kErrWaitProducer);
+            for (int k = 2 * i; k < 2 * i + 2 && ok; ++k) {
+              if (k == 0) continue;   // the spare region is always free
+              const int x = ld + k - 1;
+              ok = wait_all(bar_empty(x % C::STAGES), ((x / C::STAGES) & 1) ^ 1, kErrWaitProducer);
+            }
+            if (!ok) break;
+            if (leader) {
+              mbar_arrive_expect_tx(bar_ws(i), 2 * C::WS_PIECE_BYTES);
+              const char* src = reinterpret_cast<const char*>(p.ws_o) + (tile0 + i) * (kBM * D * 4);
+              for (int k = 2 * i; k < 2 * i + 2; ++k)
+                bulk_load(sQ + ws_piece(k, n_tiles), src + (k % 2) * C::WS_PIECE_BYTES,
+                          C::WS_PIECE_BYTES, bar_ws(i));
+            }
+            __syncwarp();
+            ws_armed = i + 1;
+          }
+        }
       } else {
         // fp32 inputs: K_j and V_j each on their own stage barrier
         for (int j = 0; j < n_tiles && ok; ++j) {
@@ -483,6 +566,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(bar_full(x % C::STAGES), 0, p.timeout_ns);
         }
       }
+      // the running-state pieces land before this CTA's shared memory is released
+      if (leader)
+        for (int i = 0; i < ws_armed; ++i) mbar_drain(bar_ws(i), 0, p.timeout_ns);
       __syncwarp();
     } else if (warp == kWarpMma) {
       // ---------------------------------------------------------- MMA issuer
@@ -771,9 +857,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      if (w.t == 0 && w.c > 0)
-        chunk_epilogue<T, D>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok, tile_id, tile_row,
-                             nullptr);
+      if (w.t == 0 && w.c > 0) {
+        const float lse_run = (w.c > 1 && row_ok) ? p.ws_lse[tile_id * kBM + tile_row] : 0.f;
+        chunk_epilogue<T, D, false>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok,
+                                    tile_id, tile_row, nullptr, lse_run, nullptr, 0u, 0u);
+      }
 
       // keys past the chunk's end, and with causal masking keys after this
       // row, are masked
@@ -840,22 +928,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
       }
       l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      // the final merge reads the running state through bulk copies: this
+      // thread's workspace stores are fenced for them a few key tiles into
+      // the last chunk, once those stores have long drained
+      const bool ws_ready =
+          kPrefetchState && r_eff > 1 && w.c == r_eff - 1 && w.t == min(2, w.nt - 1);
+      if (ws_ready) fence_proxy_async_global();
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p(wg));
+      if (lane == 0) {
+        mbar_arrive(bar_p(wg));
+        if (ws_ready) mbar_arrive(bar_ws_ready(wg));
+      }
       w.next(p);
     }
     if (ok) {
+      // (prefetching: the running state's LSE is requested before the final
+      // O is awaited)
+      const bool merge = r_eff > 1;
+      float lse_run = 0.f;
+      if (kPrefetchState && merge && row_ok) lse_run = p.ws_lse[tile_id * kBM + tile_row];
       ok = mbar_wait(bar_o(wg), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
                      kErrWaitSoftmax);
       ok = __all_sync(0xffffffffu, ok);
+      // bf16: the running state itself was fetched into shared memory
+      const bool pre = kPrefetchState && merge && q_row0 + wg * kBM < p.s_q;
+      if (ok && pre) {
+        ok = mbar_wait(bar_ws(wg), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
+                       kErrWaitSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+      }
       if (ok) {
+        if (!kPrefetchState && merge && row_ok) lse_run = p.ws_lse[tile_id * kBM + tile_row];
         tc_fence_after();
+        // (the state is read only where the epilogue merges, for rows of an
+        // existing query tile: exactly where it was prefetched)
+        const uint32_t pre0 = ws_piece(2 * wg, n_tiles), pre1 = ws_piece(2 * wg + 1, n_tiles);
         // the Q tiles are idle once every Q K has completed: each warp
         // stages its 32 output rows there (32 x D x out bytes = 8 KB)
-        chunk_epilogue<T, D>(p, tO, r_eff - 1, r_eff, m_used, l, b, h, q_row, row_ok, tile_id, tile_row,
-                             smem + warp * 32 * D * sizeof(T));
+        chunk_epilogue<T, D, kPrefetchState>(p, tO, r_eff - 1, r_eff, m_used, l, b, h, q_row,
+                                             row_ok, tile_id, tile_row,
+                                             smem + warp * 32 * D * sizeof(T), lse_run, smem,
+                                             pre0, pre1);
       }
     }
   }

@@ -165,6 +165,22 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
 }
 
 // ----------------------------------------------------------------- tcgen05
+// Orders this thread's earlier generic-proxy global accesses before later
+// async-proxy (bulk copy) accesses that synchronise with it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Untiled bulk copy global -> shared: both addresses 16-byte aligned, size a
+// multiple of 16; the barrier's transaction count drops by `bytes` on arrival.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
