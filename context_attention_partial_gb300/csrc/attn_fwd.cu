@@ -26,6 +26,9 @@
 //               -> row sum, P (bf16, or fp32 for tf32) back into S's columns;
 //               at each chunk end the normalised partial is merged in fp32
 //               with the running result (held in a global fp32 workspace).
+//   Three quarters through its key tiles, the producer also has the Q
+//   tiles of the CTA one wave later (linear block order, one CTA per SM)
+//   fetched into L2, so the next wave's start finds them there.
 //   Without causal masking (bf16), once every K/V tile is in flight the
 //   producer also bulk-copies the running result that the final merge
 //   reads into shared memory (a spare region plus three released stages),
@@ -490,6 +493,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if (ok) ld = 1;   // K_0
         for (int j = 0; j < n_tiles && ok; ++j) {
+          // three quarters through, the Q tiles of the CTA that will start
+          // one wave later (blocks are dispatched in linear order, one per
+          // SM) are fetched into L2, while HBM is otherwise little used
+          if (!GROUPED && j == (3 * n_tiles) / 4 && leader) {
+            const int64_t ln =
+                blockIdx.x +
+                static_cast<int64_t>(gridDim.x) *
+                    (blockIdx.y + static_cast<int64_t>(gridDim.y) * blockIdx.z) +
+                p.resident_ctas;
+            if (ln < static_cast<int64_t>(gridDim.x) * gridDim.y * gridDim.z) {
+              const int xn = static_cast<int>(ln % gridDim.x);
+              const int yn = static_cast<int>((ln / gridDim.x) % gridDim.y);
+              const int zn = static_cast<int>(ln / (static_cast<int64_t>(gridDim.x) * gridDim.y));
+              const int row0 = (CAUSAL ? static_cast<int>(gridDim.z) - 1 - zn : xn) * (kNT * kBM);
+              const int hn = CAUSAL ? xn : yn, bn = CAUSAL ? yn : zn;
+              for (int i = 0; i < kNT; ++i)
+                if (row0 + i * kBM < p.s_q)
+                  for (int kb = 0; kb < C::NKB; ++kb)
+                    tma_prefetch_l2_4d(&tm_q, kb * C::BOX_COLS, row0 + i * kBM, hn, bn);
+            }
+          }
           const int key_v = p.chunk_start[w.c] + w.t * kBN;
           w.next(p);
           const bool more = j + 1 < n_tiles;
@@ -999,7 +1023,19 @@ cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
   if (e != cudaSuccess) return e;
   const unsigned q_blocks = (p.s_q + kNT * kBM - 1) / (kNT * kBM);
   const dim3 grid = CAUSAL ? dim3(p.heads, p.batch, q_blocks) : dim3(q_blocks, p.heads, p.batch);
-  kernel<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, p);
+  // one CTA per SM is resident (its shared memory and registers fill one)
+  static int sms[64] = {0};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (sms[dev] == 0) {
+    e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  AttnParams pl = p;
+  pl.resident_ctas = sms[dev];
+  kernel<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, pl);
   return cudaGetLastError();
 }
 

@@ -35,6 +35,7 @@ struct AttnParams {
   int group_count;
   int group_heads;
   int n_tiles_all;       // key tiles over all chunks (the count without causal masking)
+  int resident_ctas;     // CTAs in flight at once (one per SM; set at launch)
   int chunk_start[CPATTN_MAX_RING_DEGREE + 1];
 };
 
