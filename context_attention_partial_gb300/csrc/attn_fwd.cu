@@ -28,7 +28,8 @@
 //               with the running result (held in a global fp32 workspace).
 //   Three quarters through its key tiles, the producer also has the Q
 //   tiles of the CTA one wave later (linear block order, one CTA per SM)
-//   fetched into L2, so the next wave's start finds them there.
+//   fetched into L2, so the next wave's start finds them there (bf16
+//   launches; not for Ulysses Anything's padded head slots).
 //   Without causal masking (bf16), once every K/V tile is in flight the
 //   producer also bulk-copies the running result that the final merge
 //   reads into shared memory (a spare region plus three released stages),
@@ -1024,17 +1025,8 @@ cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
   const unsigned q_blocks = (p.s_q + kNT * kBM - 1) / (kNT * kBM);
   const dim3 grid = CAUSAL ? dim3(p.heads, p.batch, q_blocks) : dim3(q_blocks, p.heads, p.batch);
   // one CTA per SM is resident (its shared memory and registers fill one)
-  static int sms[64] = {0};
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (sms[dev] == 0) {
-    e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-  }
   AttnParams pl = p;
-  pl.resident_ctas = sms[dev];
+  pl.resident_ctas = sm_count();
   kernel<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, pl);
   return cudaGetLastError();
 }

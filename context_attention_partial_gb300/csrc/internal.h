@@ -74,4 +74,7 @@ cudaError_t launch_permute_anything(const PermuteParams& p, cudaStream_t stream)
 // Error word helpers (defined with the device symbol).
 cudaError_t read_and_clear_device_error(unsigned int* value, cudaStream_t stream);
 
+// SM count of the current device (152, GB300's, if it cannot be read).
+int sm_count();
+
 }  // namespace cpattn

@@ -168,13 +168,6 @@ __global__ void __launch_bounds__(kPermuteThreads)
   }
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-  return n;
-}
-
 template <typename V>
 cudaError_t launch_permute_typed(const PermuteParams& p, int64_t total, int64_t unit,
                                  cudaStream_t stream) {
@@ -243,6 +236,13 @@ cudaError_t launch_permute_anything_typed(const PermuteParams& p, int64_t row,
 }
 
 }  // namespace
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;   // GB300's count
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 152;
+  return n;
+}
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int64_t total = p.rows * (p.head_dim / 4);
