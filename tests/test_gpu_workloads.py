@@ -12,7 +12,7 @@ import torch
 
 import context_attention_partial_gb300 as cp
 import oracle
-from context_attention_partial_gb300.workloads import WORKLOADS, make_workload
+from context_attention_partial_gb300.workloads import WORKLOADS, make_qkv, make_workload
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -35,34 +35,40 @@ def check_convex(out, v, dims):
     assert bool((o >= vmin - slack).all()) and bool((o <= vmax + slack).all())
 
 
-def run_ring_workload(name, heads_to_check):
-    w, q, k, v = make_workload(name, seed=0)
+def check_ring_sampled(name, q, k, v, ring_degree, ring_anything, causal, heads_to_check):
+    """cp.ring on q, k, v [B, H, S, D] against the oracle on sampled rows."""
+    S, D = q.shape[2], q.shape[3]
     gq, gk, gv = q.to(DEV), k.to(DEV), v.to(DEV)
-    out, lse = cp.ring(gq, gk, gv, ring_degree=w.ring_degree, ring_anything=w.ring_anything,
-                       causal=w.causal)
+    out, lse = cp.ring(gq, gk, gv, ring_degree=ring_degree, ring_anything=ring_anything,
+                       causal=causal)
     torch.cuda.synchronize()
     assert cp.last_device_status() == 0
     assert out.dtype == q.dtype and lse.dtype == torch.float32
     assert torch.isfinite(lse).all()
     check_convex(out, gv, dims=2)
-    tol_o, tol_l = (2e-3, 1e-3) if w.dtype == "f32" else (1e-2, 1e-3)
+    tol_o, tol_l = (2e-3, 1e-3) if q.dtype == torch.float32 else (1e-2, 1e-3)
     out_c, lse_c = out.cpu(), lse.cpu()
     for i, (b, h) in enumerate(heads_to_check):
-        rows = sample_rows(w.seq, i)
-        if w.causal:
+        rows = sample_rows(S, i)
+        if causal:
             # causal rows depend on their position: evaluate whole-sequence rows
             ro, rl = oracle.ring(q[b, h].unsqueeze(0), k[b, h].unsqueeze(0), v[b, h].unsqueeze(0),
-                                 w.head_dim ** -0.5, ring_degree=w.ring_degree,
-                                 ring_anything=w.ring_anything, causal=True, rows=rows)
+                                 D ** -0.5, ring_degree=ring_degree,
+                                 ring_anything=ring_anything, causal=True, rows=rows)
             ro, rl = ro[None], rl[None]
         else:
             ro, rl = oracle.ring(q[b, h, rows].unsqueeze(0), k[b, h].unsqueeze(0),
-                                 v[b, h].unsqueeze(0), w.head_dim ** -0.5,
-                                 ring_degree=w.ring_degree, ring_anything=w.ring_anything)
+                                 v[b, h].unsqueeze(0), D ** -0.5,
+                                 ring_degree=ring_degree, ring_anything=ring_anything)
         go = out_c[b, h, rows].float().numpy()
         gl = lse_c[b, h, rows].numpy()
         assert np.abs(go - ro[0]).max() <= tol_o, (name, b, h)
         assert np.abs(gl - rl[0]).max() <= tol_l, (name, b, h)
+
+
+def run_ring_workload(name, heads_to_check):
+    w, q, k, v = make_workload(name, seed=0)
+    check_ring_sampled(name, q, k, v, w.ring_degree, w.ring_anything, w.causal, heads_to_check)
 
 
 def test_tiny_ring_full():
@@ -85,6 +91,34 @@ def test_uneven_ring_sampled():
 
 def test_flux_ring_causal_sampled():
     run_ring_workload("flux_ring_causal", [(0, 0), (0, 13), (0, 23)])
+
+
+def test_ring_d64_many_waves_sampled():
+    """bf16 at D = 64 (eight K/V stages, 16 KB running-state pieces) over
+    864 CTAs, several waves: the final merge's shared-memory prefetch and the
+    next wave's Q prefetch run across wave boundaries, ring degree 3."""
+    q, k, v = make_qkv((2, 24, 4608, 64), torch.bfloat16, seed=61)
+    check_ring_sampled("d64", q, k, v, 3, False, False, [(0, 0), (1, 12), (1, 23)])
+
+
+def test_partial_flux_shape_sampled():
+    """One partial (cpattn_partial) at the FLUX shape: bf16 inputs, fp32
+    output written straight from the epilogue, fp32 LSE."""
+    w, q, k, v = make_workload("flux_ring", seed=0)
+    gv = v.to(DEV)
+    out, lse = cp.partial(q.to(DEV), k.to(DEV), gv)
+    torch.cuda.synchronize()
+    assert cp.last_device_status() == 0
+    assert out.dtype == torch.float32 and lse.dtype == torch.float32
+    assert torch.isfinite(lse).all()
+    check_convex(out, gv, dims=2)
+    out_c, lse_c = out.cpu(), lse.cpu()
+    for i, (b, h) in enumerate([(0, 0), (0, 9), (0, 23)]):
+        rows = sample_rows(w.seq, 50 + i)
+        ro, rl = oracle.partial(q[b, h, rows].unsqueeze(0), k[b, h].unsqueeze(0),
+                                v[b, h].unsqueeze(0), w.head_dim ** -0.5)
+        assert np.abs(out_c[b, h, rows].numpy() - ro[0]).max() <= 1e-2, (b, h)
+        assert np.abs(lse_c[b, h, rows].numpy() - rl[0]).max() <= 1e-3, (b, h)
 
 
 @pytest.mark.slow
