@@ -24,7 +24,8 @@ EXPORTS = (
     "cpattn_ulysses_permute", "cpattn_status_string", "cpattn_last_device_status",
     "cpattn_set_wait_timeout_ns", "cpattn_ring_noalloc", "cpattn_ring_noalloc_max_workspace_bytes",
     "cpattn_set_fault_injection", "cpattn_ring_causal", "cpattn_ulysses_anything_permute",
-    "cpattn_ulysses_anything_attention",
+    "cpattn_ulysses_anything_attention", "cpattn_ulysses_permute_batch",
+    "cpattn_ulysses_anything_permute_batch",
 )
 
 
@@ -72,6 +73,8 @@ def load():
         lib.cpattn_ring_causal.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P, vp,
                                            ctypes.c_size_t, vp]
         lib.cpattn_ulysses_anything_permute.argtypes = [P, i32, i32, P, vp]
+        lib.cpattn_ulysses_permute_batch.argtypes = [i32, P, i32, i32, P, vp]
+        lib.cpattn_ulysses_anything_permute_batch.argtypes = [i32, P, i32, i32, P, vp]
         lib.cpattn_ulysses_anything_attention.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P,
                                                           vp]
         lib.cpattn_ring_noalloc.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P, vp]
@@ -86,7 +89,8 @@ def load():
         lib.cpattn_set_fault_injection.restype = None
         for name in ("cpattn_partial", "cpattn_merge", "cpattn_ring", "cpattn_ulysses_permute",
                      "cpattn_last_device_status", "cpattn_ring_noalloc", "cpattn_ring_causal",
-                     "cpattn_ulysses_anything_permute", "cpattn_ulysses_anything_attention"):
+                     "cpattn_ulysses_anything_permute", "cpattn_ulysses_anything_attention",
+                     "cpattn_ulysses_permute_batch", "cpattn_ulysses_anything_permute_batch"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

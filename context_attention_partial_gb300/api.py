@@ -7,6 +7,7 @@ kernels; CPU tensors are rejected (there is no CPU path).
 """
 from __future__ import annotations
 
+import ctypes
 from typing import Optional, Tuple
 
 import torch
@@ -143,6 +144,34 @@ def ulysses_permute(x: torch.Tensor, degree: int, direction: int,
     return out
 
 
+def _descs(ts) -> ctypes.Array:
+    arr = (_lib.CTensor * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = _desc(t)
+    return arr
+
+
+def ulysses_permute_batch(xs, degree: int, direction: int, outs=None,
+                          stream: Optional[torch.cuda.Stream] = None) -> list:
+    """ulysses_permute of up to 4 tensors of one shape and dtype in one
+    launch (cpattn_ulysses_permute_batch); returns the outputs in order."""
+    lib = _lib.load()
+    outs = list(outs) if outs is not None else [None] * len(xs)
+    for i, x in enumerate(xs):
+        if outs[i] is None:
+            if direction == 1:
+                B, S, H, D = x.shape
+                outs[i] = torch.empty(degree, B, S, H // max(degree, 1), D, device=x.device,
+                                      dtype=x.dtype)
+            else:
+                G, B, S, Hg, D = x.shape
+                outs[i] = torch.empty(B, S, G * Hg, D, device=x.device, dtype=x.dtype)
+    check(lib.cpattn_ulysses_permute_batch(len(xs), _descs(xs), int(degree), int(direction),
+                                           _descs(outs), _stream_handle(stream)),
+          "cpattn_ulysses_permute_batch")
+    return outs
+
+
 def grouped_as_bhsd(t: torch.Tensor) -> torch.Tensor:
     """[G,B,S,H/G,D] -> strided view [G*B, H/G, S, D] (no copy)."""
     G, B, S, Hg, D = t.shape
@@ -175,9 +204,10 @@ def unified_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ulysses
         return t
 
     gshape = (G, B, S, H // max(G, 1), D)
-    qg = ulysses_permute(q, G, 1, out=buf("q", gshape, q.dtype), stream=stream)
-    kg = ulysses_permute(k, G, 1, out=buf("k", gshape, k.dtype), stream=stream)
-    vg = ulysses_permute(v, G, 1, out=buf("v", gshape, v.dtype), stream=stream)
+    # q, k and v regrouped by one launch
+    qg, kg, vg = ulysses_permute_batch(
+        (q, k, v), G, 1, outs=(buf("q", gshape, q.dtype), buf("k", gshape, q.dtype),
+                               buf("v", gshape, q.dtype)), stream=stream)
     og = buf("o", gshape, q.dtype)
     lse = buf("lse", (G * B, H // G, S), torch.float32)
     qv = grouped_as_bhsd(qg)
@@ -224,6 +254,31 @@ def ulysses_anything_permute(x: torch.Tensor, degree: int, direction: int,
     return out
 
 
+def ulysses_anything_permute_batch(xs, degree: int, direction: int, heads: Optional[int] = None,
+                                   outs=None,
+                                   stream: Optional[torch.cuda.Stream] = None) -> list:
+    """ulysses_anything_permute of up to 4 tensors of one shape and dtype in
+    one launch (cpattn_ulysses_anything_permute_batch); returns the outputs."""
+    lib = _lib.load()
+    G = int(degree)
+    outs = list(outs) if outs is not None else [None] * len(xs)
+    for i, x in enumerate(xs):
+        if outs[i] is None:
+            if direction == 1:
+                B, S, H, D = x.shape
+                outs[i] = torch.empty(G, B, S, -(-H // max(G, 1)), D, device=x.device,
+                                      dtype=x.dtype)
+            else:
+                if heads is None:
+                    raise ValueError("the inverse regroup needs heads (or outs)")
+                _, B, S, _, D = x.shape
+                outs[i] = torch.empty(B, S, int(heads), D, device=x.device, dtype=x.dtype)
+    check(lib.cpattn_ulysses_anything_permute_batch(len(xs), _descs(xs), G, int(direction),
+                                                    _descs(outs), _stream_handle(stream)),
+          "cpattn_ulysses_anything_permute_batch")
+    return outs
+
+
 def ulysses_anything_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, degree: int,
                                scale: Optional[float] = None,
                                stream: Optional[torch.cuda.Stream] = None,
@@ -249,9 +304,10 @@ def ulysses_anything_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
         return t
 
     gshape = (G, B, S, hm, D)
-    qg = ulysses_anything_permute(q, G, 1, out=buf("q", gshape, q.dtype), stream=stream)
-    kg = ulysses_anything_permute(k, G, 1, out=buf("k", gshape, k.dtype), stream=stream)
-    vg = ulysses_anything_permute(v, G, 1, out=buf("v", gshape, v.dtype), stream=stream)
+    # q, k and v regrouped by one launch
+    qg, kg, vg = ulysses_anything_permute_batch(
+        (q, k, v), G, 1, outs=(buf("q", gshape, q.dtype), buf("k", gshape, q.dtype),
+                               buf("v", gshape, q.dtype)), stream=stream)
     og = buf("o", gshape, q.dtype)
     lse = buf("lse", (G, B, hm, S), torch.float32)
     check(lib.cpattn_ulysses_anything_attention(_desc(qg), _desc(kg), _desc(vg), _scale(scale), H,

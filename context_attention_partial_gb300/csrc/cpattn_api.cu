@@ -231,6 +231,93 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
+// One Ulysses regroup pair x -> y (even: [B,S,H,D] <-> [G,B,S,H/G,D];
+// Ulysses Anything: [B,S,H,D] <-> [G,B,S,ceil(H/G),D]).  Fills dims with
+// (B, S, H, D) and bytes with the sizes of x and y.
+cpattn_status permute_pair_check(const cpattn_tensor* x, const cpattn_tensor* y, int degree,
+                                 int dir, bool anything, int64_t* dims, uintptr_t* xbytes,
+                                 uintptr_t* ybytes) {
+  if (!x || !y) return CPATTN_ERR_NULL;
+  if (!dtype_known(x->dtype) || y->dtype != x->dtype) return CPATTN_ERR_DTYPE;
+  if (dir != 1 && dir != -1) return CPATTN_ERR_SHAPE;
+  if (degree < 1) return CPATTN_ERR_SHAPE;
+  const cpattn_tensor* flat = dir == 1 ? x : y;      // [B, S, H, D]
+  const cpattn_tensor* grouped = dir == 1 ? y : x;   // [G, B, S, H/G or ceil(H/G), D]
+  if (!shape_ok(flat, 4) || !shape_ok(grouped, 5)) return CPATTN_ERR_SHAPE;
+  const int64_t B = flat->shape[0], S = flat->shape[1], H = flat->shape[2], D = flat->shape[3];
+  if (!anything && H % degree != 0) return CPATTN_ERR_DIVISIBILITY;
+  const int64_t hg = anything ? (H + degree - 1) / degree : H / degree;
+  if (grouped->shape[0] != degree || grouped->shape[1] != B || grouped->shape[2] != S ||
+      grouped->shape[3] != hg || grouped->shape[4] != D)
+    return CPATTN_ERR_SHAPE;
+  dims[0] = B;
+  dims[1] = S;
+  dims[2] = H;
+  dims[3] = D;
+  const int eb = elem_bytes(x->dtype);
+  const uintptr_t flat_bytes = static_cast<uintptr_t>(B * S * H * D * eb);
+  const uintptr_t grouped_bytes = static_cast<uintptr_t>(degree * B * S * hg * D * eb);
+  *xbytes = dir == 1 ? flat_bytes : grouped_bytes;
+  *ybytes = dir == 1 ? grouped_bytes : flat_bytes;
+  if (B * S * H * D == 0) return CPATTN_OK;
+  if (!x->data || !y->data) return CPATTN_ERR_NULL;
+  if (!contiguous(x) || !contiguous(y)) return CPATTN_ERR_LAYOUT;
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x->data), ya = reinterpret_cast<uintptr_t>(y->data);
+  if (xa % eb || ya % eb) return CPATTN_ERR_LAYOUT;
+  return CPATTN_OK;
+}
+
+bool overlaps(const void* a, uintptr_t an, const void* b, uintptr_t bn) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bn && y < x + an;
+}
+
+// n regroups of one shape and dtype in one launch; no output may overlap
+// any buffer of the call.
+cpattn_status permute_batch(int n, const cpattn_tensor* x, int degree, int dir, cpattn_tensor* y,
+                            bool anything, cudaStream_t stream) {
+  if (n < 1 || n > cpattn::kMaxPermuteBatch) return CPATTN_ERR_SHAPE;
+  if (!x || !y) return CPATTN_ERR_NULL;
+  int64_t dims[4] = {0, 0, 0, 0};
+  uintptr_t xb = 0, yb = 0;
+  for (int i = 0; i < n; ++i) {
+    int64_t d[4];
+    uintptr_t xbi = 0, ybi = 0;
+    const cpattn_status st = permute_pair_check(&x[i], &y[i], degree, dir, anything, d, &xbi, &ybi);
+    if (st != CPATTN_OK) return st;
+    if (i == 0) {
+      for (int j = 0; j < 4; ++j) dims[j] = d[j];
+      xb = xbi;
+      yb = ybi;
+    } else {
+      if (x[i].dtype != x[0].dtype) return CPATTN_ERR_DTYPE;
+      for (int j = 0; j < 4; ++j)
+        if (d[j] != dims[j]) return CPATTN_ERR_SHAPE;
+    }
+  }
+  if (dims[0] * dims[1] * dims[2] * dims[3] == 0) return CPATTN_OK;
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j)
+      if (overlaps(y[i].data, yb, x[j].data, xb) || (i != j && overlaps(y[i].data, yb, y[j].data, yb)))
+        return CPATTN_ERR_LAYOUT;
+  cpattn::PermuteParams p;
+  p.n = n;
+  for (int i = 0; i < n; ++i) {
+    p.x[i] = x[i].data;
+    p.y[i] = y[i].data;
+  }
+  p.batch = dims[0];
+  p.seq = dims[1];
+  p.heads = dims[2];
+  p.head_dim = dims[3];
+  p.degree = degree;
+  p.dir = dir;
+  p.elem_bytes = elem_bytes(x[0].dtype);
+  const cudaError_t e =
+      anything ? cpattn::launch_permute_anything(p, stream) : cpattn::launch_permute(p, stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -311,79 +398,24 @@ cpattn_status cpattn_merge(cpattn_tensor* out_a, cpattn_tensor* lse_a, const cpa
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
+cpattn_status cpattn_ulysses_permute_batch(int n, const cpattn_tensor* x, int degree, int dir,
+                                           cpattn_tensor* y, void* stream) {
+  return permute_batch(n, x, degree, dir, y, false, static_cast<cudaStream_t>(stream));
+}
+
 cpattn_status cpattn_ulysses_permute(const cpattn_tensor* x, int degree, int dir, cpattn_tensor* y,
                                      void* stream) {
-  if (!x || !y) return CPATTN_ERR_NULL;
-  if (!dtype_known(x->dtype) || y->dtype != x->dtype) return CPATTN_ERR_DTYPE;
-  if (dir != 1 && dir != -1) return CPATTN_ERR_SHAPE;
-  if (degree < 1) return CPATTN_ERR_SHAPE;
-  const cpattn_tensor* flat = dir == 1 ? x : y;      // [B, S, H, D]
-  const cpattn_tensor* grouped = dir == 1 ? y : x;   // [G, B, S, H/G, D]
-  if (!shape_ok(flat, 4) || !shape_ok(grouped, 5)) return CPATTN_ERR_SHAPE;
-  const int64_t B = flat->shape[0], S = flat->shape[1], H = flat->shape[2], D = flat->shape[3];
-  if (H % degree != 0) return CPATTN_ERR_DIVISIBILITY;
-  if (grouped->shape[0] != degree || grouped->shape[1] != B || grouped->shape[2] != S ||
-      grouped->shape[3] != H / degree || grouped->shape[4] != D)
-    return CPATTN_ERR_SHAPE;
-  if (B * S * H * D == 0) return CPATTN_OK;
-  if (!x->data || !y->data) return CPATTN_ERR_NULL;
-  if (!contiguous(x) || !contiguous(y)) return CPATTN_ERR_LAYOUT;
-  const int eb = elem_bytes(x->dtype);
-  const uintptr_t xa = reinterpret_cast<uintptr_t>(x->data), ya = reinterpret_cast<uintptr_t>(y->data);
-  if (xa % eb || ya % eb) return CPATTN_ERR_LAYOUT;
-  const uintptr_t bytes = static_cast<uintptr_t>(B * S * H * D * eb);
-  if (xa < ya + bytes && ya < xa + bytes) return CPATTN_ERR_LAYOUT;   // overlap
-  cpattn::PermuteParams p;
-  p.x = x->data;
-  p.y = y->data;
-  p.batch = B;
-  p.seq = S;
-  p.heads = H;
-  p.head_dim = D;
-  p.degree = degree;
-  p.dir = dir;
-  p.elem_bytes = eb;
-  const cudaError_t e = cpattn::launch_permute(p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  return permute_batch(1, x, degree, dir, y, false, static_cast<cudaStream_t>(stream));
+}
+
+cpattn_status cpattn_ulysses_anything_permute_batch(int n, const cpattn_tensor* x, int degree,
+                                                    int dir, cpattn_tensor* y, void* stream) {
+  return permute_batch(n, x, degree, dir, y, true, static_cast<cudaStream_t>(stream));
 }
 
 cpattn_status cpattn_ulysses_anything_permute(const cpattn_tensor* x, int degree, int dir,
                                               cpattn_tensor* y, void* stream) {
-  if (!x || !y) return CPATTN_ERR_NULL;
-  if (!dtype_known(x->dtype) || y->dtype != x->dtype) return CPATTN_ERR_DTYPE;
-  if (dir != 1 && dir != -1) return CPATTN_ERR_SHAPE;
-  if (degree < 1) return CPATTN_ERR_SHAPE;
-  const cpattn_tensor* flat = dir == 1 ? x : y;      // [B, S, H, D]
-  const cpattn_tensor* grouped = dir == 1 ? y : x;   // [G, B, S, ceil(H/G), D]
-  if (!shape_ok(flat, 4) || !shape_ok(grouped, 5)) return CPATTN_ERR_SHAPE;
-  const int64_t B = flat->shape[0], S = flat->shape[1], H = flat->shape[2], D = flat->shape[3];
-  const int64_t hm = (H + degree - 1) / degree;
-  if (grouped->shape[0] != degree || grouped->shape[1] != B || grouped->shape[2] != S ||
-      grouped->shape[3] != hm || grouped->shape[4] != D)
-    return CPATTN_ERR_SHAPE;
-  if (B * S * H * D == 0) return CPATTN_OK;
-  if (!x->data || !y->data) return CPATTN_ERR_NULL;
-  if (!contiguous(x) || !contiguous(y)) return CPATTN_ERR_LAYOUT;
-  const int eb = elem_bytes(x->dtype);
-  const uintptr_t xa = reinterpret_cast<uintptr_t>(x->data), ya = reinterpret_cast<uintptr_t>(y->data);
-  if (xa % eb || ya % eb) return CPATTN_ERR_LAYOUT;
-  const uintptr_t flat_bytes = static_cast<uintptr_t>(B * S * H * D * eb);
-  const uintptr_t grouped_bytes = static_cast<uintptr_t>(degree * B * S * hm * D * eb);
-  const uintptr_t xb = dir == 1 ? flat_bytes : grouped_bytes;
-  const uintptr_t yb = dir == 1 ? grouped_bytes : flat_bytes;
-  if (xa < ya + yb && ya < xa + xb) return CPATTN_ERR_LAYOUT;   // overlap
-  cpattn::PermuteParams p;
-  p.x = x->data;
-  p.y = y->data;
-  p.batch = B;
-  p.seq = S;
-  p.heads = H;
-  p.head_dim = D;
-  p.degree = degree;
-  p.dir = dir;
-  p.elem_bytes = eb;
-  const cudaError_t e = cpattn::launch_permute_anything(p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  return permute_batch(1, x, degree, dir, y, true, static_cast<cudaStream_t>(stream));
 }
 
 cpattn_status cpattn_ulysses_anything_attention(const cpattn_tensor* q, const cpattn_tensor* k,

@@ -59,9 +59,13 @@ struct MergeParams {
 };
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 
+// Up to kMaxPermuteBatch tensors of one shape and dtype regrouped by one
+// launch (tensor i: x[i] -> y[i]).
+constexpr int kMaxPermuteBatch = CPATTN_MAX_PERMUTE_BATCH;
 struct PermuteParams {
-  const void* x;
-  void* y;
+  int n;
+  const void* x[kMaxPermuteBatch];
+  void* y[kMaxPermuteBatch];
   int64_t batch, seq, heads, head_dim, degree;
   int dir;               // +1 forward, -1 inverse
   int elem_bytes;

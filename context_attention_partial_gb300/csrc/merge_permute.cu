@@ -98,10 +98,31 @@ __device__ __forceinline__ Index source_of(Index idx, Index unit, Index bs, Inde
   return src_seg * unit + w;
 }
 
+// The tensors of one launch: grid row blockIdx.y (even regroup) or slice
+// blockIdx.z (Ulysses Anything) selects one.
+template <typename V>
+struct PermutePtrs {
+  const V* x[kMaxPermuteBatch];
+  V* y[kMaxPermuteBatch];
+};
+
+// Tensor t's pointers through fixed indices (the parameter block is not
+// indexed at run time).
+template <typename V>
+__device__ __forceinline__ void permute_pick(const PermutePtrs<V>& p, unsigned t, const V*& x,
+                                             V*& y) {
+  static_assert(kMaxPermuteBatch == 4, "one select per tensor slot");
+  x = t == 0 ? p.x[0] : t == 1 ? p.x[1] : t == 2 ? p.x[2] : p.x[3];
+  y = t == 0 ? p.y[0] : t == 1 ? p.y[1] : t == 2 ? p.y[2] : p.y[3];
+}
+
 template <typename V, typename Index>
 __global__ void __launch_bounds__(kPermuteThreads)
-    permute_kernel(const V* __restrict__ x, V* __restrict__ y, Index total, Index unit, Index bs,
-                   Index g, int dir) {
+    permute_kernel(const PermutePtrs<V> ptrs, Index total, Index unit, Index bs, Index g,
+                   int dir) {
+  const V* x;
+  V* y;
+  permute_pick(ptrs, blockIdx.y, x, y);
   const Index stride = static_cast<Index>(gridDim.x) * blockDim.x;
   for (Index base = static_cast<Index>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
        base += stride * kUnroll) {
@@ -129,9 +150,11 @@ __global__ void __launch_bounds__(kPermuteThreads)
 // padded to hm = ceil(H/G) slots.
 template <typename V, typename Index, bool POW2>
 __global__ void __launch_bounds__(kPermuteThreads)
-    permute_anything_kernel(const V* __restrict__ x, V* __restrict__ y, Index per_head,
-                            Index row, int row_shift, Index heads, Index hm, Index bs, Index q,
-                            Index r, int dir) {
+    permute_anything_kernel(const PermutePtrs<V> ptrs, Index per_head, Index row, int row_shift,
+                            Index heads, Index hm, Index bs, Index q, Index r, int dir) {
+  const V* x;
+  V* y;
+  permute_pick(ptrs, blockIdx.z, x, y);
   const Index h = blockIdx.y;
   const Index big = r * (q + 1);
   Index g, j;
@@ -169,21 +192,32 @@ __global__ void __launch_bounds__(kPermuteThreads)
 }
 
 template <typename V>
+PermutePtrs<V> permute_ptrs(const PermuteParams& p) {
+  PermutePtrs<V> ptrs{};
+  for (int i = 0; i < p.n; ++i) {
+    ptrs.x[i] = static_cast<const V*>(p.x[i]);
+    ptrs.y[i] = static_cast<V*>(p.y[i]);
+  }
+  return ptrs;
+}
+
+template <typename V>
 cudaError_t launch_permute_typed(const PermuteParams& p, int64_t total, int64_t unit,
                                  cudaStream_t stream) {
   const int64_t bs = p.batch * p.seq;
   const int64_t want = (total + kPermuteThreads * kUnroll - 1) / (kPermuteThreads * kUnroll);
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  // about 8 blocks of 256 threads per SM in total, shared by the tensors
+  const int64_t cap = (static_cast<int64_t>(sm_count()) * 8 + p.n - 1) / p.n;
   const int blocks = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
-  const V* x = static_cast<const V*>(p.x);
-  V* y = static_cast<V*>(p.y);
+  const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(p.n));
+  const PermutePtrs<V> ptrs = permute_ptrs<V>(p);
   if (total + static_cast<int64_t>(blocks) * kPermuteThreads * kUnroll < (int64_t(1) << 31))
-    permute_kernel<V, uint32_t><<<blocks, kPermuteThreads, 0, stream>>>(
-        x, y, static_cast<uint32_t>(total), static_cast<uint32_t>(unit),
+    permute_kernel<V, uint32_t><<<grid, kPermuteThreads, 0, stream>>>(
+        ptrs, static_cast<uint32_t>(total), static_cast<uint32_t>(unit),
         static_cast<uint32_t>(bs), static_cast<uint32_t>(p.degree), p.dir);
   else
-    permute_kernel<V, uint64_t><<<blocks, kPermuteThreads, 0, stream>>>(
-        x, y, static_cast<uint64_t>(total), static_cast<uint64_t>(unit),
+    permute_kernel<V, uint64_t><<<grid, kPermuteThreads, 0, stream>>>(
+        ptrs, static_cast<uint64_t>(total), static_cast<uint64_t>(unit),
         static_cast<uint64_t>(bs), static_cast<uint64_t>(p.degree), p.dir);
   return cudaGetLastError();
 }
@@ -196,16 +230,15 @@ cudaError_t launch_permute_anything_index(const PermuteParams& p, int64_t per_he
   const int64_t q = p.heads / p.degree, r = p.heads % p.degree;
   int shift = 0;
   while ((int64_t(1) << shift) < row) ++shift;
-  const V* x = static_cast<const V*>(p.x);
-  V* y = static_cast<V*>(p.y);
+  const PermutePtrs<V> ptrs = permute_ptrs<V>(p);
   if ((int64_t(1) << shift) == row)
     permute_anything_kernel<V, Index, true><<<grid, kPermuteThreads, 0, stream>>>(
-        x, y, static_cast<Index>(per_head), static_cast<Index>(row), shift,
+        ptrs, static_cast<Index>(per_head), static_cast<Index>(row), shift,
         static_cast<Index>(p.heads), static_cast<Index>(hm), static_cast<Index>(bs),
         static_cast<Index>(q), static_cast<Index>(r), p.dir);
   else
     permute_anything_kernel<V, Index, false><<<grid, kPermuteThreads, 0, stream>>>(
-        x, y, static_cast<Index>(per_head), static_cast<Index>(row), shift,
+        ptrs, static_cast<Index>(per_head), static_cast<Index>(row), shift,
         static_cast<Index>(p.heads), static_cast<Index>(hm), static_cast<Index>(bs),
         static_cast<Index>(q), static_cast<Index>(r), p.dir);
   return cudaGetLastError();
@@ -218,13 +251,15 @@ cudaError_t launch_permute_anything_typed(const PermuteParams& p, int64_t row,
   const int64_t hm = (p.heads + p.degree - 1) / p.degree;
   const int64_t per_head = bs * row;   // units of one head
   // about 8 blocks of 256 threads per SM in total, spread over the heads
+  // and the tensors
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
-  int64_t bx = (cap + p.heads - 1) / p.heads;
+  int64_t bx = (cap + p.heads * p.n - 1) / (p.heads * p.n);
   const int64_t want = (per_head + kPermuteThreads * kUnroll - 1) / (kPermuteThreads * kUnroll);
   if (bx > want) bx = want;
   if (bx < 1) bx = 1;
   if (p.heads > 65535) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(p.heads));
+  const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(p.heads),
+                  static_cast<unsigned>(p.n));
   // largest index on either side, and the loop counter's reach
   const int64_t flat_total = bs * p.heads * row;
   const int64_t grouped_total = p.degree * bs * hm * row;
@@ -254,13 +289,21 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// every tensor's base 16-byte aligned (the vector paths)
+static bool all_aligned16(const PermuteParams& p) {
+  for (int i = 0; i < p.n; ++i)
+    if (reinterpret_cast<uintptr_t>(p.x[i]) % 16 != 0 || reinterpret_cast<uintptr_t>(p.y[i]) % 16 != 0)
+      return false;
+  return true;
+}
+
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream) {
+  if (p.n < 1 || p.n > kMaxPermuteBatch) return cudaErrorInvalidValue;
   const int64_t seg_elems = (p.heads / p.degree) * p.head_dim;
   const int64_t total_elems = p.batch * p.seq * p.heads * p.head_dim;
   if (total_elems == 0) return cudaSuccess;
   const int64_t seg_bytes = seg_elems * p.elem_bytes;
-  const bool vec = seg_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(p.x) % 16 == 0 &&
-                   reinterpret_cast<uintptr_t>(p.y) % 16 == 0;
+  const bool vec = seg_bytes % 16 == 0 && all_aligned16(p);
   if (vec)
     return launch_permute_typed<uint4>(p, total_elems * p.elem_bytes / 16, seg_bytes / 16, stream);
   if (p.elem_bytes == 2)
@@ -271,11 +314,11 @@ cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_permute_anything(const PermuteParams& p, cudaStream_t stream) {
+  if (p.n < 1 || p.n > kMaxPermuteBatch) return cudaErrorInvalidValue;
   const int64_t total_elems = p.batch * p.seq * p.heads * p.head_dim;
   if (total_elems == 0) return cudaSuccess;
   const int64_t row_bytes = p.head_dim * p.elem_bytes;
-  const bool vec = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(p.x) % 16 == 0 &&
-                   reinterpret_cast<uintptr_t>(p.y) % 16 == 0;
+  const bool vec = row_bytes % 16 == 0 && all_aligned16(p);
   if (vec) return launch_permute_anything_typed<uint4>(p, row_bytes / 16, stream);
   if (p.elem_bytes == 2) return launch_permute_anything_typed<unsigned short>(p, p.head_dim, stream);
   if (p.elem_bytes == 4) return launch_permute_anything_typed<unsigned int>(p, p.head_dim, stream);

@@ -170,6 +170,23 @@ cpattn_status cpattn_ring_causal(const cpattn_tensor* q, const cpattn_tensor* k,
 cpattn_status cpattn_ulysses_permute(const cpattn_tensor* x, int degree,
                                      int dir, cpattn_tensor* y, void* stream);
 
+/* Up to CPATTN_MAX_PERMUTE_BATCH regroups in one launch. */
+#define CPATTN_MAX_PERMUTE_BATCH 4
+
+/*
+ * cpattn_ulysses_permute_batch -- cpattn_ulysses_permute of n tensors of one
+ * shape and dtype in one launch (q, k and v each pass through the all-to-all
+ * of [CP] "Ulysses Attention" before the per-group attention).
+ *   x, y: arrays of n descriptors; pair i is regrouped x[i] -> y[i] exactly
+ *   as cpattn_ulysses_permute does, 1 <= n <= CPATTN_MAX_PERMUTE_BATCH
+ *   (else CPATTN_ERR_SHAPE).  Every pair must have the shapes and dtype of
+ *   pair 0 (else CPATTN_ERR_SHAPE / CPATTN_ERR_DTYPE); no output may overlap
+ *   any input or another output (CPATTN_ERR_LAYOUT).  Other errors as
+ *   cpattn_ulysses_permute; on any error nothing is launched.
+ */
+cpattn_status cpattn_ulysses_permute_batch(int n, const cpattn_tensor* x, int degree,
+                                           int dir, cpattn_tensor* y, void* stream);
+
 /*
  * cpattn_ulysses_anything_permute -- the head regroup of Ulysses Anything
  * ([CP] "Ulysses Anything Attention", [API] ulysses_anything: Ulysses without
@@ -189,6 +206,15 @@ cpattn_status cpattn_ulysses_permute(const cpattn_tensor* x, int degree,
 cpattn_status cpattn_ulysses_anything_permute(const cpattn_tensor* x,
                                               int degree, int dir,
                                               cpattn_tensor* y, void* stream);
+
+/*
+ * cpattn_ulysses_anything_permute_batch -- cpattn_ulysses_anything_permute
+ * of n tensors of one shape and dtype in one launch; arguments, pairing and
+ * errors as cpattn_ulysses_permute_batch.
+ */
+cpattn_status cpattn_ulysses_anything_permute_batch(int n, const cpattn_tensor* x,
+                                                    int degree, int dir,
+                                                    cpattn_tensor* y, void* stream);
 
 /*
  * cpattn_ulysses_anything_attention -- attention of every Ulysses Anything

@@ -122,6 +122,43 @@ def test_permute_validation():
                                       4, 1, y, None) == LAYOUT
 
 
+def test_permute_batch_validation():
+    """The batched regroups check every pair as the single call does, and
+    that the pairs share one shape and dtype and no output overlaps another
+    buffer of the call."""
+    lib = cp.load_library()
+    arr = lambda *ts: (_lib.CTensor * len(ts))(*ts)
+    mb = 1 << 24
+    for batch, h_slots, deg in ((lib.cpattn_ulysses_permute_batch, 6, 4),
+                                (lib.cpattn_ulysses_anything_permute_batch, 5, 5)):
+        gshape = (deg, 1, 16, h_slots, 128)
+        xs = arr(*(t((1, 16, 24, 128), data=FAKE + i * mb) for i in range(3)))
+        ys = arr(*(t(gshape, data=FAKE + (8 + i) * mb) for i in range(3)))
+        assert batch(0, xs, deg, 1, ys, None) == SHAPE
+        assert batch(5, xs, deg, 1, ys, None) == SHAPE
+        assert batch(3, None, deg, 1, ys, None) == NULL
+        # a pair whose shapes differ from pair 0's
+        assert batch(3, xs, deg, 1, arr(ys[0], ys[1], t((deg, 1, 8, h_slots, 128),
+                                                          data=FAKE + 10 * mb)), None) == SHAPE
+        x_short = arr(xs[0], xs[1], t((1, 8, 24, 128), data=FAKE + 2 * mb))
+        assert batch(3, x_short, deg, 1, arr(ys[0], ys[1], t((deg, 1, 8, h_slots, 128),
+                                                            data=FAKE + 10 * mb)), None) == SHAPE
+        # a pair of another dtype
+        assert batch(2, arr(xs[0], t((1, 16, 24, 128), _lib.F32, data=FAKE + mb)), deg, 1,
+                     arr(ys[0], t(gshape, _lib.F32, data=FAKE + 9 * mb)), None) == DTYPE
+        # an output over another pair's input, or over another output
+        assert batch(2, arr(xs[0], xs[1]), deg, 1, arr(ys[0], t(gshape, data=FAKE + 64)),
+                     None) == LAYOUT
+        assert batch(2, arr(xs[0], xs[1]), deg, 1, arr(ys[0], t(gshape, data=FAKE + 8 * mb + 64)),
+                     None) == LAYOUT
+        # every pair is checked like the single call
+        assert batch(2, arr(xs[0], xs[1]), 0, 1, arr(ys[0], ys[1]), None) == SHAPE
+        # nothing to move: accepted without a launch
+        z = arr(t((1, 0, 24, 128), data=0), t((1, 0, 24, 128), data=0))
+        zy = arr(t((deg, 1, 0, h_slots, 128), data=0), t((deg, 1, 0, h_slots, 128), data=0))
+        assert batch(2, z, deg, 1, zy, None) == OK
+
+
 def test_ulysses_anything_validation():
     lib = cp.load_library()
     x = t((1, 16, 24, 128)); y = t((5, 1, 16, 5, 128), data=FAKE + (1 << 24))

@@ -55,6 +55,53 @@ def test_permute_bit_exact(shape, g, dtype):
     assert torch.equal(back.cpu(), oracle.ulysses_permute(ref, g, -1))
 
 
+@pytest.mark.parametrize("shape,g,dtype,n", [
+    ((1, 4608, 24, 128), 4, torch.bfloat16, 3),   # q, k, v of the Ulysses workload
+    ((2, 37, 12, 64), 3, torch.bfloat16, 2),
+    ((2, 3, 10, 3), 5, torch.bfloat16, 4),        # element path, the most tensors
+    ((1, 9, 7, 5), 7, torch.float32, 1),
+])
+def test_permute_batch_bit_exact(shape, g, dtype, n):
+    """n regroups in one launch equal n single regroups and the oracle."""
+    xs = [make_qkv(shape, dtype, seed=70 + i)[0] for i in range(n)]
+    ys = cp.ulysses_permute_batch([x.to(DEV) for x in xs], g, 1)
+    torch.cuda.synchronize()
+    for x, y in zip(xs, ys):
+        assert torch.equal(y.cpu(), oracle.ulysses_permute(x, g, 1))
+    backs = cp.ulysses_permute_batch(ys, g, -1)
+    torch.cuda.synchronize()
+    for x, back in zip(xs, backs):
+        assert torch.equal(back.cpu(), x)
+
+
+@pytest.mark.parametrize("shape,g,dtype,n", [
+    ((1, 4608, 24, 128), 5, torch.bfloat16, 3),   # q, k, v of the Ulysses Anything workload
+    ((2, 37, 7, 64), 3, torch.bfloat16, 2),
+    ((2, 3, 5, 3), 2, torch.bfloat16, 4),         # element path
+    ((1, 9, 2, 5), 4, torch.float32, 3),          # H < G
+])
+def test_anything_permute_batch_bit_exact(shape, g, dtype, n):
+    xs = [make_qkv(shape, dtype, seed=80 + i)[0] for i in range(n)]
+    H = shape[2]
+    hm = -(-H // g)
+    outs = [torch.full((g,) + shape[:2] + (hm, shape[3]), -3.0, dtype=dtype, device=DEV)
+            for _ in range(n)]
+    ys = cp.ulysses_anything_permute_batch([x.to(DEV) for x in xs], g, 1, outs=outs)
+    torch.cuda.synchronize()
+    start = oracle.ulysses_anything_heads(H, g)
+    for x, y in zip(xs, ys):
+        ref = oracle.ulysses_anything_permute(x, g, 1)
+        yc = y.cpu()
+        for gi in range(g):
+            hg = start[gi + 1] - start[gi]
+            assert torch.equal(yc[gi, :, :, :hg], ref[gi, :, :, :hg])
+            assert torch.all(yc[gi, :, :, hg:] == -3.0)        # padding not written
+    backs = cp.ulysses_anything_permute_batch(ys, g, -1, heads=H)
+    torch.cuda.synchronize()
+    for x, back in zip(xs, backs):
+        assert torch.equal(back.cpu(), x)
+
+
 def test_permute_rejects_indivisible_heads():
     x = torch.zeros(1, 4, 6, 8, device=DEV, dtype=torch.bfloat16)
     with pytest.raises(cp.CpattnError) as e:
