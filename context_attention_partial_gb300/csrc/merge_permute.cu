@@ -206,8 +206,10 @@ cudaError_t launch_permute_typed(const PermuteParams& p, int64_t total, int64_t 
                                  cudaStream_t stream) {
   const int64_t bs = p.batch * p.seq;
   const int64_t want = (total + kPermuteThreads * kUnroll - 1) / (kPermuteThreads * kUnroll);
-  // about 8 blocks of 256 threads per SM in total, shared by the tensors
-  const int64_t cap = (static_cast<int64_t>(sm_count()) * 8 + p.n - 1) / p.n;
+  // about 32 blocks of 256 threads per SM in total (8 resident at a time),
+  // shared by the tensors: the finer split evens out the tail of a batch
+  // (three tensors: 29.8 us with 8, 27.0 us with 32; one tensor unchanged)
+  const int64_t cap = (static_cast<int64_t>(sm_count()) * 32 + p.n - 1) / p.n;
   const int blocks = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
   const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(p.n));
   const PermutePtrs<V> ptrs = permute_ptrs<V>(p);
@@ -250,9 +252,9 @@ cudaError_t launch_permute_anything_typed(const PermuteParams& p, int64_t row,
   const int64_t bs = p.batch * p.seq;
   const int64_t hm = (p.heads + p.degree - 1) / p.degree;
   const int64_t per_head = bs * row;   // units of one head
-  // about 8 blocks of 256 threads per SM in total, spread over the heads
-  // and the tensors
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  // about 32 blocks of 256 threads per SM in total, spread over the heads
+  // and the tensors (as for the even regroup)
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 32;
   int64_t bx = (cap + p.heads * p.n - 1) / (p.heads * p.n);
   const int64_t want = (per_head + kPermuteThreads * kUnroll - 1) / (kPermuteThreads * kUnroll);
   if (bx > want) bx = want;
