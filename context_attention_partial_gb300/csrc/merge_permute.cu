@@ -285,7 +285,9 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int64_t total = p.rows * (p.head_dim / 4);
   if (total == 0) return cudaSuccess;
   const int64_t want = (total + kMergeThreads - 1) / kMergeThreads;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  // about 32 blocks of 256 threads per SM in total (8 resident at a time):
+  // FLUX shape 28.7-29.0 us with 8, 27.3-27.4 us with 32
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 32;
   const int blocks = static_cast<int>(want < cap ? want : cap);
   merge_kernel<<<blocks, kMergeThreads, 0, stream>>>(p);
   return cudaGetLastError();
