@@ -100,6 +100,42 @@ def ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ring_degree: int = 1
     return out, lse
 
 
+def prepare_ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ring_degree: int = 1,
+                 ring_anything: bool = False, scale: Optional[float] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None, causal: bool = False):
+    """``ring`` with its argument descriptors built once: returns a callable
+    that issues the same cpattn_ring (or cpattn_ring_causal) call on the
+    same tensors and stream each time it is called, so repeated steps cost
+    one foreign-function call of host time.  The callable's ``out`` and
+    ``lse`` attributes are the output tensors; it keeps every tensor it was
+    given alive."""
+    lib = _lib.load()
+    B, H, S, D = q.shape
+    if out is None:
+        out = torch.empty(B, H, S, D, device=q.device, dtype=q.dtype)
+    if lse is None:
+        lse = torch.empty(B, H, S, device=q.device, dtype=torch.float32)
+    need = ring_workspace_bytes(q, ring_degree)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    fn = lib.cpattn_ring_causal if causal else lib.cpattn_ring
+    name = "cpattn_ring_causal" if causal else "cpattn_ring"
+    args = (_desc(q), _desc(k), _desc(v), _scale(scale), int(ring_degree),
+            int(bool(ring_anything)), _desc(out), _desc(lse), ws_ptr, ws_bytes,
+            _stream_handle(stream))
+
+    def call():
+        check(fn(*args), name)
+
+    call.out, call.lse = out, lse
+    call.keep = (q, k, v, out, lse, workspace)
+    return call
+
+
 def ring_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ring_degree: int = 1,
                  ring_anything: bool = False, scale: Optional[float] = None,
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
@@ -219,6 +255,36 @@ def unified_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ulysses
     return out, lse
 
 
+def prepare_unified(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ulysses_degree: int,
+                    ring_degree: int = 1, scale: Optional[float] = None,
+                    stream: Optional[torch.cuda.Stream] = None, causal: bool = False):
+    """``unified_attention`` with its buffers allocated and its three calls'
+    descriptors built once (batched regroup of q, k, v; ring over the grouped
+    view; inverse regroup).  Returns a callable issuing the three calls; its
+    ``out`` and ``lse`` attributes are the results."""
+    lib = _lib.load()
+    B, S, H, D = q.shape
+    G, R = int(ulysses_degree), int(ring_degree)
+    gshape = (G, B, S, H // max(G, 1), D)
+    qg, kg, vg, og = (torch.empty(gshape, device=q.device, dtype=q.dtype) for _ in range(4))
+    lse = torch.empty(G * B, H // G, S, device=q.device, dtype=torch.float32)
+    out = torch.empty(B, S, H, D, device=q.device, dtype=q.dtype)
+    h = _stream_handle(stream)
+    fwd = (3, _descs((q, k, v)), G, 1, _descs((qg, kg, vg)), h)
+    inner = prepare_ring(grouped_as_bhsd(qg), grouped_as_bhsd(kg), grouped_as_bhsd(vg), R, False,
+                         scale, out=grouped_as_bhsd(og), lse=lse, stream=stream, causal=causal)
+    inv = (_desc(og), G, -1, _desc(out), h)
+
+    def call():
+        check(lib.cpattn_ulysses_permute_batch(*fwd), "cpattn_ulysses_permute_batch")
+        inner()
+        check(lib.cpattn_ulysses_permute(*inv), "cpattn_ulysses_permute")
+
+    call.out, call.lse = out, lse
+    call.keep = (q, k, v, qg, kg, vg, og, inner)
+    return call
+
+
 def ulysses_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, degree: int,
                       scale: Optional[float] = None,
                       stream: Optional[torch.cuda.Stream] = None,
@@ -318,6 +384,37 @@ def ulysses_anything_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     return out, lse
 
 
+def prepare_ulysses_anything(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, degree: int,
+                             scale: Optional[float] = None,
+                             stream: Optional[torch.cuda.Stream] = None, causal: bool = False):
+    """``ulysses_anything_attention`` with its buffers allocated and its
+    three calls' descriptors built once; returns a callable issuing them,
+    whose ``out`` and ``lse`` attributes are the results."""
+    lib = _lib.load()
+    B, S, H, D = q.shape
+    G = int(degree)
+    hm = -(-H // max(G, 1))
+    gshape = (G, B, S, hm, D)
+    qg, kg, vg, og = (torch.empty(gshape, device=q.device, dtype=q.dtype) for _ in range(4))
+    lse = torch.empty(G, B, hm, S, device=q.device, dtype=torch.float32)
+    out = torch.empty(B, S, H, D, device=q.device, dtype=q.dtype)
+    h = _stream_handle(stream)
+    fwd = (3, _descs((q, k, v)), G, 1, _descs((qg, kg, vg)), h)
+    attn = (_desc(qg), _desc(kg), _desc(vg), _scale(scale), H, int(bool(causal)), _desc(og),
+            _desc(lse), h)
+    inv = (_desc(og), G, -1, _desc(out), h)
+
+    def call():
+        check(lib.cpattn_ulysses_anything_permute_batch(*fwd),
+              "cpattn_ulysses_anything_permute_batch")
+        check(lib.cpattn_ulysses_anything_attention(*attn), "cpattn_ulysses_anything_attention")
+        check(lib.cpattn_ulysses_anything_permute(*inv), "cpattn_ulysses_anything_permute")
+
+    call.out, call.lse = out, lse
+    call.keep = (q, k, v, qg, kg, vg, og)
+    return call
+
+
 def last_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronises the stream and returns (and clears) the device error word
     status: 0 = ok, 9 = a kernel-side wait timed out."""
@@ -328,7 +425,8 @@ def set_wait_timeout_ns(ns: int) -> None:
     _lib.load().cpattn_set_wait_timeout_ns(int(ns))
 
 
-__all__ = ["partial", "merge", "ring", "ring_workspace_bytes", "ring_noalloc",
+__all__ = ["partial", "merge", "ring", "ring_workspace_bytes", "ring_noalloc", "prepare_ring",
+           "prepare_unified", "prepare_ulysses_anything",
            "ring_noalloc_max_workspace_bytes", "ulysses_permute", "unified_attention",
            "ulysses_attention", "grouped_as_bhsd", "last_device_status", "set_wait_timeout_ns",
            "CpattnError"]

@@ -43,6 +43,7 @@
 //   happens in TMEM, after the previous P V has completed.
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "internal.h"
@@ -1013,15 +1014,24 @@ cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
                         const AttnParams& p, cudaStream_t stream) {
   using C = Cfg<T, D>;
   auto kernel = attn_fwd_kernel<T, D, CAUSAL, GROUPED>;
-  // The setmaxnreg split assumes exactly kLaunchRegs registers per thread at
-  // launch; with fewer, the softmax warpgroups' increase could never be
-  // granted.  Refuse to launch such a build.
-  cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+  // Once per device and instantiation: the setmaxnreg split assumes exactly
+  // kLaunchRegs registers per thread at launch (with fewer, the softmax
+  // warpgroups' increase could never be granted: refuse to launch such a
+  // build), and the dynamic shared-memory limit is raised.
+  static std::atomic<unsigned long long> ready{0};   // bit d: device d is set up
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit == 0 || (ready.load(std::memory_order_acquire) & bit) == 0) {
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kernel);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    ready.fetch_or(bit, std::memory_order_acq_rel);
+  }
   const unsigned q_blocks = (p.s_q + kNT * kBM - 1) / (kNT * kBM);
   const dim3 grid = CAUSAL ? dim3(p.heads, p.batch, q_blocks) : dim3(q_blocks, p.heads, p.batch);
   // one CTA per SM is resident (its shared memory and registers fill one)

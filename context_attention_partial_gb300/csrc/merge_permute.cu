@@ -2,8 +2,9 @@
 //
 // merge: LSE merge of two fp32 partials, in place into (o_a, lse_a)
 //   (Diffusers "Parallelism" API, ContextParallelConfig convert_to_fp32:
-//   output and LSE converted to fp32 "for ring attention numerical
-//   stability"; the formula follows from the definition of LSE):
+//   each ring step's output and LSE are held in fp32 while they are
+//   combined, to keep the combination stable; the formula follows from the
+//   definition of LSE):
 //     lse = max(a, b) + log1p(exp(min(a, b) - max(a, b)))
 //     o   = exp(a - lse) o_a + exp(b - lse) o_b,   (0, -inf) if both empty.
 //   One thread per 16-byte vector of a row; the D/4 threads of a row sit in

@@ -94,8 +94,8 @@ cpattn_status cpattn_partial(const cpattn_tensor* q, const cpattn_tensor* k,
 
 /*
  * cpattn_merge -- LSE merge of two partials over disjoint key sets, in place
- * into (out_a, lse_a) ([API] convert_to_fp32, "for ring attention numerical
- * stability"):
+ * into (out_a, lse_a) ([API] convert_to_fp32: the ring's partials are kept
+ * in fp32 while they are combined, for stability):
  *   lse = max(a, b) + log1p(exp(min(a, b) - max(a, b)))
  *   out = exp(a - lse) out_a + exp(b - lse) out_b
  * lse = -inf marks an empty partial; two empty partials give (0, -inf).

@@ -155,8 +155,9 @@ int cpo_partial_rows(const double* q, const double* k, const double* v,
 
 /* ---------------------------------------------------------------------------
  * 3. LSE merge of two partials over disjoint key sets ([API]
- *    convert_to_fp32, "for ring attention numerical stability").  The pages
- *    print no formula; it follows from the definition of LSE:
+ *    convert_to_fp32: the ring steps' outputs and LSEs are combined in fp32
+ *    for stability).  The pages print no formula; it follows from the
+ *    definition of LSE:
  *      lse = log(e^a + e^b) = max(a,b) + log1p(exp(min(a,b) - max(a,b)))
  *      o   = e^(a - lse) o_a + e^(b - lse) o_b
  *    lse = -inf marks an empty partial (the identity); two empty partials

@@ -15,7 +15,7 @@ import torch
 
 import context_attention_partial_gb300 as cp
 import oracle
-from context_attention_partial_gb300.workloads import make_partials, make_qkv
+from workloads import make_partials, make_qkv
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -240,9 +240,12 @@ def test_ring_large_scores_exercise_rescale():
     v = torch.randn(1, 2, 1024, 128, generator=g).to(torch.bfloat16)
     out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=2)
     torch.cuda.synchronize()
+    status_ok()
     ro, rl = oracle.ring(q, k, v, 128 ** -0.5, ring_degree=2)
     assert maxabs(out, ro) <= 2e-2
-    assert maxabs(lse, rl) <= 1e-3 * max(1.0, float(np.abs(rl).max()) / 8)
+    # the LSE bound stays the stated 1e-3 absolute: the scores are exact
+    # products of bf16 values summed in fp32 (error ~1e-5 at |lse| ~ 40)
+    assert maxabs(lse, rl) <= 1e-3
 
 
 def test_ring_closed_forms():
@@ -427,3 +430,31 @@ def test_ulysses_anything_leaves_padding_slots_alone():
     status_ok()
     assert torch.all(og[2, :, :, 1] == 7.0) and torch.all(lse[2, :, 1] == 9.0)
     assert torch.all(torch.isfinite(og[:2].float())) and not torch.any(lse[:2] == 9.0)
+
+
+def test_prepared_calls_equal_plain_calls():
+    """prepare_ring / prepare_unified / prepare_ulysses_anything issue the
+    same library calls with descriptors built once: bit-equal results."""
+    q, k, v = make_qkv((1, 3, 300, 128), torch.bfloat16, seed=59, device=DEV)
+    ref = cp.ring(q, k, v, 3, causal=True)
+    call = cp.prepare_ring(q, k, v, 3, causal=True)
+    call()
+    call()
+    torch.cuda.synchronize()
+    status_ok()
+    assert torch.equal(call.out, ref[0]) and torch.equal(call.lse, ref[1])
+    x = make_qkv((1, 257, 6, 64), torch.bfloat16, seed=61, device=DEV)
+    ref = cp.unified_attention(*x, 2, 2)
+    call = cp.prepare_unified(*x, 2, 2)
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(call.out, ref[0]) and torch.equal(call.lse, ref[1])
+    ref = cp.ulysses_anything_attention(*x, 4)
+    call = cp.prepare_ulysses_anything(*x, 4)
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(call.out, ref[0])
+    start = oracle.ulysses_anything_heads(6, 4)
+    for g in range(4):
+        hg = start[g + 1] - start[g]
+        assert torch.equal(call.lse[g, :, :hg], ref[1][g, :, :hg])

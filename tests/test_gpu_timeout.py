@@ -9,7 +9,7 @@ import torch
 
 import context_attention_partial_gb300 as cp
 import oracle
-from context_attention_partial_gb300.workloads import make_qkv
+from workloads import make_qkv
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"

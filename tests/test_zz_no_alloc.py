@@ -15,7 +15,7 @@ import torch
 
 import context_attention_partial_gb300 as cp
 from context_attention_partial_gb300 import _lib
-from context_attention_partial_gb300.workloads import make_qkv
+from workloads import make_qkv
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"

@@ -1,8 +1,9 @@
 """Seeded synthetic workloads.
 
 Shapes, dtypes and degrees of the workloads, and the seeded generator of
-their inputs.  This module holds none of the attention arithmetic: it is the
-one piece that both the CUDA path and the CPU oracle are fed from.
+their inputs.  This module holds none of the attention arithmetic and imports
+neither the library nor the oracle: it is the one piece that both the CUDA
+path (through the tests and the benchmark) and the CPU oracle are fed from.
 
 Input recipe: ``torch.Generator('cpu').manual_seed(seed)`` (seed 0 by
 default), then ``q, k, v = randn(shape, float32)`` drawn in that order, then a
