@@ -59,8 +59,6 @@ __device__ unsigned int g_cpattn_device_error = 0;
 namespace {
 
 constexpr int kBM = 128;          // query rows per tile (TMEM lanes)
-constexpr int kNT = 2;            // query tiles per CTA
-constexpr int kBN = 128;          // keys per K/V tile
 constexpr int kThreads = 384;     // 3 warpgroups
 constexpr int kWarpProducer = 8;  // warpgroup 2: producer, MMA, V transposer, spare
 constexpr int kWarpMma = 9;
@@ -80,11 +78,16 @@ template <typename T, int D>
 struct Cfg {
   static constexpr int ES = sizeof(T);
   static constexpr bool TF32 = (ES == 4);
+  // query tiles per CTA and keys per K/V tile: two 128-row query tiles
+  // against 128-key tiles, except for fp32 inputs with D = 128, whose tiles
+  // fit shared memory and TMEM only as one query tile against 64-key tiles
+  static constexpr int NT = (TF32 && D == 128) ? 1 : 2;
+  static constexpr int BN = (TF32 && D == 128) ? 64 : 128;
   static constexpr int ROW_BYTES = D * ES;
   static constexpr int NKB = ROW_BYTES / 128;       // 128-byte column blocks per row
   static constexpr int BOX_COLS = 128 / ES;         // elements per column block
   static constexpr int Q_TILE_BYTES = kBM * ROW_BYTES;
-  static constexpr int KV_TILE_BYTES = kBN * ROW_BYTES;
+  static constexpr int KV_TILE_BYTES = BN * ROW_BYTES;
   // fp32 inputs: the tf32 MMA kind takes no MN-major B operand, so V tiles
   // are transposed into K-major copies (rows = D, 128-byte blocks of 32
   // keys), double-buffered.  Q K^T runs as three tf32 products,
@@ -92,39 +95,40 @@ struct Cfg {
   // mantissa bits cleared), which keeps scores to about 2^-20 relative; Q_lo
   // sits in TMEM, K_lo in one shared-memory tile.
   static constexpr int VT_BUFS = TF32 ? 2 : 0;
-  static constexpr int VT_TILE_BYTES = D * kBN * ES;
+  static constexpr int VT_TILE_BYTES = D * BN * ES;
   static constexpr int KLO_BYTES = TF32 ? KV_TILE_BYTES : 0;
   static constexpr int SMEM_BUDGET = (TF32 ? 226 : 220) * 1024;
   static constexpr int STAGES_FIT =
-      (SMEM_BUDGET - kNT * Q_TILE_BYTES - VT_BUFS * VT_TILE_BYTES - KLO_BYTES) / KV_TILE_BYTES;
+      (SMEM_BUDGET - NT * Q_TILE_BYTES - VT_BUFS * VT_TILE_BYTES - KLO_BYTES) / KV_TILE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   // bf16 without causal masking: the final merge's running state (fp32,
-  // kNT query tiles x D) is fetched into shared memory as 2 kNT pieces of
+  // NT query tiles x D) is fetched into shared memory as 2 NT pieces of
   // one K/V tile's size each (half of D of one query tile): one into a
   // region of its own, the others into the stages released first once
   // every K/V tile is in flight
   static constexpr int WS_PIECE_BYTES = kBM * (D / 2) * 4;
   static constexpr int WSX_BYTES = TF32 ? 0 : WS_PIECE_BYTES;
   static constexpr int NUM_BARS =
-      1 + 2 * STAGES + 3 * kNT + 1 + 2 * VT_BUFS + (TF32 ? 3 : 0) + 2 * kNT;
-  static constexpr int SMEM_BYTES = 1024 + kNT * Q_TILE_BYTES + STAGES * KV_TILE_BYTES +
+      1 + 2 * STAGES + 3 * NT + 1 + 2 * VT_BUFS + (TF32 ? 3 : 0) + 2 * NT;
+  static constexpr int SMEM_BYTES = 1024 + NT * Q_TILE_BYTES + STAGES * KV_TILE_BYTES +
                                     VT_BUFS * VT_TILE_BYTES + KLO_BYTES + WSX_BYTES +
                                     NUM_BARS * 8 + 16;
   static constexpr int KSTEP = 32 / ES;             // K elements per MMA (32 bytes)
   static constexpr int QK_STEPS = ROW_BYTES / 32;
-  static constexpr int PV_STEPS = kBN / KSTEP;
+  static constexpr int PV_STEPS = BN / KSTEP;
   static constexpr int P_COLS_PER_STEP = KSTEP * ES / 4;
   static constexpr uint32_t FMT = TF32 ? 2u : 1u;   // tf32 : bf16
-  static constexpr uint32_t IDESC_QK = make_idesc(FMT, false, kBM, kBN);
+  static constexpr uint32_t IDESC_QK = make_idesc(FMT, false, kBM, BN);
   static constexpr uint32_t IDESC_PV = make_idesc(FMT, !TF32, kBM, D);
-  static constexpr int O_COL = kNT * kBN;
-  static constexpr int QLO_COL = O_COL + kNT * D;   // fp32 inputs: Q_lo of tile i at + i*D
+  static constexpr int O_COL = NT * BN;
+  static constexpr int QLO_COL = O_COL + NT * D;   // fp32 inputs: Q_lo of tile i at + i*D
   static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte blocks");
-  static_assert(O_COL + kNT * D <= (int)kTmemCols, "TMEM budget");
-  static_assert(!TF32 || (D == 64 && QLO_COL + kNT * D <= (int)kTmemCols), "tf32 TMEM budget");
+  static_assert(O_COL + NT * D <= (int)kTmemCols, "TMEM budget");
+  static_assert(!TF32 || QLO_COL + NT * D <= (int)kTmemCols, "tf32 TMEM budget");
+  static_assert(TF32 || (NT == 2 && BN == 128), "the bf16 MMA schedule ping-pongs two tiles");
   static_assert(!TF32 || STAGES % 2 == 0, "fp32 inputs keep K tiles on even stages");
   static_assert(STAGES >= 2, "need at least two K/V stages");
-  static_assert(TF32 || (WS_PIECE_BYTES == KV_TILE_BYTES && STAGES >= 2 * kNT),
+  static_assert(TF32 || (WS_PIECE_BYTES == KV_TILE_BYTES && STAGES >= 2 * NT),
                 "running-state pieces reuse K/V stages");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -149,14 +153,16 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int b, int rows) {
 // Walks the (chunk, tile) sequence shared by all roles.
 // The key tiles of chunk c this CTA visits: all of them, or with causal
 // masking only those starting at or before `kmax`, the CTA's last query row.
+template <int BN>
 __device__ __forceinline__ int chunk_tiles(const AttnParams& p, int c, int kmax) {
   const int end = min(p.chunk_start[c + 1], kmax + 1);
-  return end > p.chunk_start[c] ? ceil_div(end - p.chunk_start[c], kBN) : 0;
+  return end > p.chunk_start[c] ? ceil_div(end - p.chunk_start[c], BN) : 0;
 }
 
 // Walks the (chunk, tile) sequence shared by all roles; r_eff chunks (with
 // causal masking the chunks past the CTA's last query row are empty for
 // every row here, identities of the merge, and are not visited).
+template <int BN>
 struct TileWalk {
   int c = 0, t = 0, nt = 0, kmax = 0, r_eff = 0;
   __device__ void start(const AttnParams& p, int kmax_, int r_eff_) {
@@ -164,16 +170,36 @@ struct TileWalk {
     t = 0;
     kmax = kmax_;
     r_eff = r_eff_;
-    nt = chunk_tiles(p, 0, kmax);
+    nt = chunk_tiles<BN>(p, 0, kmax);
   }
   __device__ void next(const AttnParams& p) {
     if (++t == nt) {
       ++c;
       t = 0;
-      if (c < r_eff) nt = chunk_tiles(p, c, kmax);
+      if (c < r_eff) nt = chunk_tiles<BN>(p, c, kmax);
     }
   }
 };
+
+// Largest of the first `valid` scores of this thread's row; the others are
+// set to -inf in place (keys past a chunk's end or, causal, after the row).
+template <int N>
+__device__ __forceinline__ float masked_row_max(uint32_t (&s)[N], int valid) {
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (i >= valid) s[i] = f2u(-INFINITY);
+  float mx[4] = {u2f(s[0]), u2f(s[1]), u2f(s[2]), u2f(s[3])};
+#pragma unroll
+  for (int i = 4; i < N; i += 8) {
+    mx[0] = fmax3(mx[0], u2f(s[i + 0]), u2f(s[i + 1]));
+    mx[1] = fmax3(mx[1], u2f(s[i + 2]), u2f(s[i + 3]));
+    if (i + 4 < N) {
+      mx[2] = fmax3(mx[2], u2f(s[i + 4]), u2f(s[i + 5]));
+      mx[3] = fmax3(mx[3], u2f(s[i + 6]), u2f(s[i + 7]));
+    }
+  }
+  return fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
+}
 
 // Multiplies this thread's O row (TMEM) by `factor`.
 template <int D>
@@ -220,7 +246,8 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
   }
   // O columns per part: halves, or quarters when the running state comes
   // from shared memory (it is read in the same pass, so the part is smaller)
-  constexpr int NPARTS = PRE ? 4 : 2;
+  // or when a row holds more than 64 fp32 values
+  constexpr int NPARTS = (PRE || sizeof(T) * D > 256) ? 4 : 2;
   constexpr int HC = D / NPARTS;
   const int lane = tile_row % 32;
   // the final output goes through the warp's staging area when its element
@@ -339,11 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
 
   const uint32_t sQ = smem_addr(smem);
-  const uint32_t sKV = sQ + kNT * C::Q_TILE_BYTES;
+  const uint32_t sKV = sQ + C::NT * C::Q_TILE_BYTES;
   const uint32_t sVt = sKV + C::STAGES * C::KV_TILE_BYTES;
   const uint32_t sKlo = sVt + C::VT_BUFS * C::VT_TILE_BYTES;
   const uint32_t sWsx = sKlo + C::KLO_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kNT * C::Q_TILE_BYTES +
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::NT * C::Q_TILE_BYTES +
                                                C::STAGES * C::KV_TILE_BYTES +
                                                C::VT_BUFS * C::VT_TILE_BYTES + C::KLO_BYTES +
                                                C::WSX_BYTES);
@@ -352,19 +379,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto bar_empty = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
   auto bar_s = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + i); };
-  auto bar_p = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + kNT + i); };
-  auto bar_o = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + 2 * kNT + i); };
-  const uint32_t BAR_DRAIN = bar0 + 8u * (1 + 2 * C::STAGES + 3 * kNT);
-  auto bar_vt_full = [&](int i) { return bar0 + 8u * (2 + 2 * C::STAGES + 3 * kNT + i); };
+  auto bar_p = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + C::NT + i); };
+  auto bar_o = [&](int i) { return bar0 + 8u * (1 + 2 * C::STAGES + 2 * C::NT + i); };
+  const uint32_t BAR_DRAIN = bar0 + 8u * (1 + 2 * C::STAGES + 3 * C::NT);
+  auto bar_vt_full = [&](int i) { return bar0 + 8u * (2 + 2 * C::STAGES + 3 * C::NT + i); };
   auto bar_vt_empty = [&](int i) {
-    return bar0 + 8u * (2 + 2 * C::STAGES + 3 * kNT + C::VT_BUFS + i);
+    return bar0 + 8u * (2 + 2 * C::STAGES + 3 * C::NT + C::VT_BUFS + i);
   };
-  const uint32_t BAR_QLO = bar0 + 8u * (2 + 2 * C::STAGES + 3 * kNT + 2 * C::VT_BUFS);
+  const uint32_t BAR_QLO = bar0 + 8u * (2 + 2 * C::STAGES + 3 * C::NT + 2 * C::VT_BUFS);
   const uint32_t BAR_KLO_FULL = BAR_QLO + 8u;
   const uint32_t BAR_KLO_EMPTY = BAR_QLO + 16u;
-  auto bar_ws = [&](int i) { return bar0 + 8u * (C::NUM_BARS - 2 * kNT + i); };
+  auto bar_ws = [&](int i) { return bar0 + 8u * (C::NUM_BARS - 2 * C::NT + i); };
   // the running state of query tile i is written and fenced for the bulk copy
-  auto bar_ws_ready = [&](int i) { return bar0 + 8u * (C::NUM_BARS - kNT + i); };
+  auto bar_ws_ready = [&](int i) { return bar0 + 8u * (C::NUM_BARS - C::NT + i); };
   // home of piece k of the final merge's running state (query tile k / 2,
   // half k % 2 of D) with n key tiles: the spare region, then the stages of
   // K/V loads 2n, 2n + 1, ..., whose previous tiles are released first
@@ -384,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // causal: grid (H, B, query blocks), the heaviest query blocks first
   const int q_row0 =
       (CAUSAL ? static_cast<int>(gridDim.z - 1 - blockIdx.z) : static_cast<int>(blockIdx.x)) *
-      (kNT * kBM);
+      (C::NT * kBM);
   const int h = CAUSAL ? blockIdx.x : blockIdx.y;
   const int b = CAUSAL ? blockIdx.y : blockIdx.z;
   if constexpr (GROUPED) {
@@ -403,13 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // fp32 inputs: a K stage is released by the MMA and by the K_lo pass
       mbar_init(bar_empty(s), (C::TF32 && s % 2 == 0) ? 2 : 1);
     }
-    for (int i = 0; i < kNT; ++i) {
+    for (int i = 0; i < C::NT; ++i) {
       mbar_init(bar_s(i), 1);
       mbar_init(bar_p(i), 4);   // one arrival per softmax warp
       mbar_init(bar_o(i), 1);
     }
     mbar_init(BAR_DRAIN, 1);
-    for (int i = 0; i < kNT; ++i) {
+    for (int i = 0; i < C::NT; ++i) {
       mbar_init(bar_ws(i), 1);
       mbar_init(bar_ws_ready(i), 4);   // one arrival per softmax warp
     }
@@ -418,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_vt_empty(i), 1);
     }
     if (C::TF32) {
-      mbar_init(BAR_QLO, 8);   // one arrival per softmax warp
+      mbar_init(BAR_QLO, 4 * C::NT);   // one arrival per softmax warp
       mbar_init(BAR_KLO_FULL, 1);
       mbar_init(BAR_KLO_EMPTY, 1);
     }
@@ -426,15 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     // The Q tiles (and, bf16, the first K tile) are requested before the
     // block-wide barrier, so their latency overlaps the rest of the setup.
-    mbar_arrive_expect_tx(BAR_Q, kNT * C::Q_TILE_BYTES);
-    for (int i = 0; i < kNT; ++i)
+    mbar_arrive_expect_tx(BAR_Q, C::NT * C::Q_TILE_BYTES);
+    for (int i = 0; i < C::NT; ++i)
       for (int kb = 0; kb < C::NKB; ++kb)
         tma_load_4d(sQ + i * C::Q_TILE_BYTES + kb * kBM * 128, &tm_q, BAR_Q, kb * C::BOX_COLS,
                     q_row0 + i * kBM, h, b);
     if (!C::TF32 && p.fault_skip_kv == 0) {
       mbar_arrive_expect_tx(bar_full(0), C::KV_TILE_BYTES);
       for (int kb = 0; kb < C::NKB; ++kb)
-        tma_load_4d(sKV + kb * kBN * 128, &tm_k, bar_full(0), kb * C::BOX_COLS, p.chunk_start[0], h,
+        tma_load_4d(sKV + kb * C::BN * 128, &tm_k, bar_full(0), kb * C::BOX_COLS, p.chunk_start[0], h,
                     b);
     }
   }
@@ -452,13 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // largest key index a row of this CTA may attend; chunks starting past it
   // are skipped (chunk 0 starts at key 0, so at least one chunk remains)
   // (INT_MAX - 1 without causal masking, so that kmax + 1 cannot overflow)
-  const int kmax = CAUSAL ? min(q_row0 + kNT * kBM, p.s_q) - 1 : 0x7ffffffe;
+  const int kmax = CAUSAL ? min(q_row0 + C::NT * kBM, p.s_q) - 1 : 0x7ffffffe;
   int r_eff = p.ring_degree;
   int n_tiles = p.n_tiles_all;   // (computed by the host without causal masking)
   if (CAUSAL) {
     while (r_eff > 1 && p.chunk_start[r_eff - 1] > kmax) --r_eff;
     n_tiles = 0;
-    for (int c = 0; c < r_eff; ++c) n_tiles += chunk_tiles(p, c, kmax);
+    for (int c = 0; c < r_eff; ++c) n_tiles += chunk_tiles<C::BN>(p, c, kmax);
   }
 
   if (warp >= 8) {
@@ -480,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // fault injection (testing): no K/V copies, so every consumer's
       // bounded wait runs out and the CTA takes the abort path
       bool ok = p.fault_skip_kv == 0;
-      TileWalk w;
+      TileWalk<C::BN> w;
       w.start(p, kmax, r_eff);
       if constexpr (!C::TF32) {
         // bf16: K_0 alone, then V_j and K_{j+1} as one pair on K_{j+1}'s
@@ -490,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         static_assert(C::STAGES % 2 == 0, "K/V pairing needs an even stage count");
         auto load = [&](const CUtensorMap* tm, int stage, uint32_t bar, int key0) {
           for (int kb = 0; kb < C::NKB; ++kb)
-            tma_load_4d(sKV + stage * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar,
+            tma_load_4d(sKV + stage * C::KV_TILE_BYTES + kb * C::BN * 128, tm, bar,
                         kb * C::BOX_COLS, key0, h, b);
         };
         if (ok) ld = 1;   // K_0
@@ -508,18 +535,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int xn = static_cast<int>(ln % gridDim.x);
               const int yn = static_cast<int>((ln / gridDim.x) % gridDim.y);
               const int zn = static_cast<int>(ln / (static_cast<int64_t>(gridDim.x) * gridDim.y));
-              const int row0 = (CAUSAL ? static_cast<int>(gridDim.z) - 1 - zn : xn) * (kNT * kBM);
+              const int row0 = (CAUSAL ? static_cast<int>(gridDim.z) - 1 - zn : xn) * (C::NT * kBM);
               const int hn = CAUSAL ? xn : yn, bn = CAUSAL ? yn : zn;
-              for (int i = 0; i < kNT; ++i)
+              for (int i = 0; i < C::NT; ++i)
                 if (row0 + i * kBM < p.s_q)
                   for (int kb = 0; kb < C::NKB; ++kb)
                     tma_prefetch_l2_4d(&tm_q, kb * C::BOX_COLS, row0 + i * kBM, hn, bn);
             }
           }
-          const int key_v = p.chunk_start[w.c] + w.t * kBN;
+          const int key_v = p.chunk_start[w.c] + w.t * C::BN;
           w.next(p);
           const bool more = j + 1 < n_tiles;
-          const int key_k = more ? p.chunk_start[w.c] + w.t * kBN : 0;
+          const int key_k = more ? p.chunk_start[w.c] + w.t * C::BN : 0;
           const int sv = ld % C::STAGES, sk = (ld + 1) % C::STAGES;
           ok = wait_all(bar_empty(sv), ((ld / C::STAGES) & 1) ^ 1, kErrWaitProducer);
           if (ok && more)
@@ -540,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kPrefetchState && ok && r_eff > 1) {
           const int64_t tile0 =
               (static_cast<int64_t>(b) * p.heads + h) * ((p.s_q + kBM - 1) / kBM) + q_row0 / kBM;
-          for (int i = 0; i < kNT && ok; ++i) {
+          for (int i = 0; i < C::NT && ok; ++i) {
             if (q_row0 + i * kBM >= p.s_q) break;   // no such query tile, no state
             ok = wait_all(bar_ws_ready(i), 0, kErrWaitProducer);
             for (int k = 2 * i; k < 2 * i + 2 && ok; ++k) {
@@ -563,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // fp32 inputs: K_j and V_j each on their own stage barrier
         for (int j = 0; j < n_tiles && ok; ++j) {
-          const int key0 = p.chunk_start[w.c] + w.t * kBN;
+          const int key0 = p.chunk_start[w.c] + w.t * C::BN;
           for (int which = 0; which < 2; ++which) {
             const int s = ld % C::STAGES;
             const uint32_t ph = (ld / C::STAGES) & 1;
@@ -573,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(bar_full(s), C::KV_TILE_BYTES);
               const CUtensorMap* tm = which == 0 ? &tm_k : &tm_v;
               for (int kb = 0; kb < C::NKB; ++kb)
-                tma_load_4d(sKV + s * C::KV_TILE_BYTES + kb * kBN * 128, tm, bar_full(s),
+                tma_load_4d(sKV + s * C::KV_TILE_BYTES + kb * C::BN * 128, tm, bar_full(s),
                             kb * C::BOX_COLS, key0, h, b);
             }
             __syncwarp();
@@ -602,17 +629,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // compile-time offset (byte offset >> 4).
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(sKV, 16, 1024);
-      const uint64_t v_desc = smem_desc_sw128(sKV, kBN * 128, 1024);
+      const uint64_t v_desc = smem_desc_sw128(sKV, C::BN * 128, 1024);
       const uint64_t vt_desc = C::TF32 ? smem_desc_sw128(sVt, 16, 1024) : 0;
       const uint64_t klo_desc = C::TF32 ? smem_desc_sw128(sKlo, 16, 1024) : 0;
       auto issue_qk = [&](int i, int stage) {
-        const uint32_t d_tmem = tmem + i * kBN;
+        const uint32_t d_tmem = tmem + i * C::BN;
         const uint64_t a0 = q_desc + static_cast<uint64_t>((i * C::Q_TILE_BYTES) >> 4);
         const uint64_t b0 = k_desc + static_cast<uint64_t>((stage * C::KV_TILE_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::QK_STEPS; ++kk) {
           const uint64_t off_a = ((kk / 4) * (kBM * 128) + (kk % 4) * 32) >> 4;
-          const uint64_t off_b = ((kk / 4) * (kBN * 128) + (kk % 4) * 32) >> 4;
+          const uint64_t off_b = ((kk / 4) * (C::BN * 128) + (kk % 4) * 32) >> 4;
           mma_ss<C::TF32>(d_tmem, a0 + off_a, b0 + off_b, C::IDESC_QK, kk > 0);
           if constexpr (C::TF32) {
             mma_ss<true>(d_tmem, a0 + off_a, klo_desc + off_b, C::IDESC_QK, 1u);
@@ -625,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // TMA tile; tf32 reads the transposed, K-major copy.
       auto issue_pv = [&](int i, uint64_t b0, uint32_t acc) {
         const uint32_t d_tmem = tmem + C::O_COL + i * D;
-        const uint32_t a_tmem = tmem + i * kBN;
+        const uint32_t a_tmem = tmem + i * C::BN;
 #pragma unroll
         for (int kk = 0; kk < C::PV_STEPS; ++kk) {
           uint64_t off_b;
@@ -644,16 +671,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         if (leader) {
-          issue_qk(0, 0);
-          mma_commit(bar_s(0));
-          issue_qk(1, 0);
-          mma_commit(bar_s(1));
+#pragma unroll
+          for (int i = 0; i < C::NT; ++i) {
+            issue_qk(i, 0);
+            mma_commit(bar_s(i));
+          }
           mma_commit(bar_empty(0));
           if constexpr (C::TF32) mma_commit(BAR_KLO_EMPTY);
         }
         __syncwarp();
       }
-      TileWalk w;
+      TileWalk<C::BN> w;
       w.start(p, kmax, r_eff);
       for (int j = 0; j < n_tiles && ok; ++j) {
         const uint32_t acc = w.t != 0 ? 1u : 0u;
@@ -690,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-            kd[kk] = kb + (((kk / 4) * (kBN * 128) + (kk % 4) * 32) >> 4);
+            kd[kk] = kb + (((kk / 4) * (C::BN * 128) + (kk % 4) * 32) >> 4);
             qd[kk] = static_cast<uint32_t>(q_desc) + (((kk / 4) * (kBM * 128) + (kk % 4) * 32) >> 4);
           }
           ok = __all_sync(0xffffffffu, kv_now) || wait_all(kv_bar, kv_ph, kErrWaitMma);
@@ -714,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           // query tile 1: P in the next S columns, Q in the next tile
 #pragma unroll
-          for (int kk = 0; kk < C::PV_STEPS; ++kk) pa[kk] += kBN;
+          for (int kk = 0; kk < C::PV_STEPS; ++kk) pa[kk] += C::BN;
 #pragma unroll
           for (int kk = 0; kk < C::QK_STEPS; ++kk) qd[kk] += C::Q_TILE_BYTES >> 4;
           ok = __all_sync(0xffffffffu, p1_now) || wait_all(bar_p(1), j & 1, kErrWaitMma);
@@ -724,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_group<C::PV_STEPS, false>(tmem + C::O_COL + D, pa, vd, hi, C::IDESC_PV, acc);
             mma_commit(bar_empty(sv));
             if (more) {
-              mma_group<C::QK_STEPS, true>(tmem + kBN, qd, kd, hi, C::IDESC_QK, 0u);
+              mma_group<C::QK_STEPS, true>(tmem + C::BN, qd, kd, hi, C::IDESC_QK, 0u);
               mma_commit(bar_s(1));
               mma_commit(bar_empty(sk));
             } else {
@@ -732,43 +760,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          // fp32 inputs (3 MMAs per step): query tile 0, every wait of the
-          // group (P_0, transposed V_j, K_{j+1} and its low part) before the
-          // first MMA
-          ok = wait_all(bar_p(0), j & 1, kErrWaitMma);
-          if (!ok) break;
-          ok = wait_all(bar_vt_full(j & 1), (j >> 1) & 1, kErrWaitMma);
+          // fp32 inputs (3 MMAs per Q K step), query tile by query tile; the
+          // first tile's group waits for everything it reads (P_0, the
+          // transposed V_j, K_{j+1} and its low part) before its first MMA,
+          // the last tile's group releases V_j's copy, K_{j+1} and K_lo
           const uint64_t v_base = vt_desc + static_cast<uint64_t>(((j & 1) * C::VT_TILE_BYTES) >> 4);
-          if (ok && more) ok = wait_all(bar_full(sk), phk, kErrWaitMma);
-          if (ok && more) ok = wait_all(BAR_KLO_FULL, (j + 1) & 1, kErrWaitMma);
-          if (!ok) break;
-          tc_fence_after();
-          if (leader) {
-            issue_pv(0, v_base, acc);
-            if (more) {
-              issue_qk(0, sk);
-              mma_commit(bar_s(0));
-            } else {
-              mma_commit(bar_o(0));
+#pragma unroll
+          for (int i = 0; i < C::NT && ok; ++i) {
+            ok = wait_all(bar_p(i), j & 1, kErrWaitMma);
+            if (ok && i == 0) ok = wait_all(bar_vt_full(j & 1), (j >> 1) & 1, kErrWaitMma);
+            if (ok && i == 0 && more) ok = wait_all(bar_full(sk), phk, kErrWaitMma);
+            if (ok && i == 0 && more) ok = wait_all(BAR_KLO_FULL, (j + 1) & 1, kErrWaitMma);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) {
+              const bool last_tile = i == C::NT - 1;
+              issue_pv(i, v_base, acc);
+              if (last_tile) mma_commit(bar_vt_empty(j & 1));
+              if (more) {
+                issue_qk(i, sk);
+                mma_commit(bar_s(i));
+                if (last_tile) {
+                  mma_commit(bar_empty(sk));
+                  mma_commit(BAR_KLO_EMPTY);
+                }
+              } else {
+                mma_commit(bar_o(i));
+              }
             }
+            __syncwarp();
           }
-          __syncwarp();
-          // query tile 1
-          ok = wait_all(bar_p(1), j & 1, kErrWaitMma);
           if (!ok) break;
-          tc_fence_after();
-          if (leader) {
-            issue_pv(1, v_base, acc);
-            mma_commit(bar_vt_empty(j & 1));
-            if (more) {
-              issue_qk(1, sk);
-              mma_commit(bar_s(1));
-              mma_commit(bar_empty(sk));
-              mma_commit(BAR_KLO_EMPTY);
-            } else {
-              mma_commit(bar_o(1));
-            }
-          }
         }
         __syncwarp();
         w.next(p);
@@ -819,9 +841,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const uint8_t* src = smem + (sKV - sQ) + sv * C::KV_TILE_BYTES;
         uint8_t* dst = smem + (sVt - sQ) + (j & 1) * C::VT_TILE_BYTES;
-        for (int e = lane; e < kBN * D; e += 32) {
-          const int key = e % kBN, d = e / kBN;
-          const uint32_t v = *reinterpret_cast<const uint32_t*>(src + sw128_offset(key, d * 4, kBN));
+        for (int e = lane; e < C::BN * D; e += 32) {
+          const int key = e % C::BN, d = e / C::BN;
+          const uint32_t v = *reinterpret_cast<const uint32_t*>(src + sw128_offset(key, d * 4, C::BN));
           *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = v & 0xFFFFE000u;
         }
         fence_proxy_async_smem();
@@ -833,13 +855,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-  } else {
+  } else if (warp / 4 < C::NT) {
     // ------------------------------------------------------------ softmax
+    // (one warpgroup per query tile; with a single query tile per CTA the
+    // second softmax warpgroup has no work and waits at the final barrier)
     regs_increase<kSoftmaxRegs>();
     const int wg = warp / 4;
     const int quarter = warp % 4;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + wg * kBN;
+    const uint32_t tS = tmem + lane_base + wg * C::BN;
     const uint32_t tO = tmem + lane_base + C::O_COL + wg * D;
     const int q_row = q_row0 + wg * kBM + quarter * 32 + lane;
     // this row's query tile in the running-state workspace, and its row there
@@ -867,15 +891,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           lo[d] = f2u(u2f(x) - u2f(hi));
         }
         fence_proxy_async_smem();
-        tmem_st_x64(tmem + lane_base + C::QLO_COL + wg * D,
-                    *reinterpret_cast<uint32_t(*)[64]>(&lo[0]));
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 64)
+          tmem_st_x64(tmem + lane_base + C::QLO_COL + wg * D + c0,
+                      *reinterpret_cast<uint32_t(*)[64]>(&lo[c0]));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR_QLO);
       }
     }
-    TileWalk w;
+    TileWalk<C::BN> w;
     w.start(p, kmax, r_eff);
     for (int j = 0; j < n_tiles && ok; ++j) {
       ok = mbar_wait(bar_s(wg), j & 1, abort_flag, p.timeout_ns, &g_cpattn_device_error,
@@ -891,31 +917,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // keys past the chunk's end, and with causal masking keys after this
       // row, are masked
-      const int key0 = p.chunk_start[w.c] + w.t * kBN;
+      const int key0 = p.chunk_start[w.c] + w.t * C::BN;
       int valid = p.chunk_start[w.c + 1] - key0;
       if constexpr (CAUSAL) valid = min(valid, q_row + 1 - key0);
-      const bool masked = CAUSAL ? __any_sync(0xffffffffu, valid < kBN) : valid < kBN;
-      uint32_t s[kBN];
+      const bool masked = CAUSAL ? __any_sync(0xffffffffu, valid < C::BN) : valid < C::BN;
+      uint32_t s[C::BN];
       float row_max;
-      if (!masked) {
-        // the TMEM load returns the row max as well (no max pass)
-        tmem_ld_max_x128(tS, s, row_max);
-      } else {
-        tmem_ld_x128(tS, s);
-#pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (i >= valid) s[i] = f2u(-INFINITY);
-        float mx[4] = {u2f(s[0]), u2f(s[1]), u2f(s[2]), u2f(s[3])};
-#pragma unroll
-        for (int i = 4; i < kBN; i += 8) {
-          mx[0] = fmax3(mx[0], u2f(s[i + 0]), u2f(s[i + 1]));
-          mx[1] = fmax3(mx[1], u2f(s[i + 2]), u2f(s[i + 3]));
-          if (i + 4 < kBN) {
-            mx[2] = fmax3(mx[2], u2f(s[i + 4]), u2f(s[i + 5]));
-            mx[3] = fmax3(mx[3], u2f(s[i + 6]), u2f(s[i + 7]));
-          }
+      if constexpr (C::BN == 128) {
+        if (!masked) {
+          // the TMEM load returns the row max as well (no max pass)
+          tmem_ld_max_x128(tS, s, row_max);
+        } else {
+          tmem_ld_x128(tS, s);
+          row_max = masked_row_max<C::BN>(s, valid);
         }
-        row_max = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
+      } else {
+        tmem_ld_x64(tS, s);
+        row_max = masked_row_max<C::BN>(s, masked ? valid : C::BN);
       }
       const float m_tile = row_max * sl2;
       float factor = 1.f;
@@ -935,7 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float neg_m = (CAUSAL && m_used == -INFINITY) ? 0.f : -m_used;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < kBN / 2; ++i) {
+      for (int i = 0; i < C::BN / 2; ++i) {
         float x0, x1;
         ffma2(x0, x1, u2f(s[2 * i]), u2f(s[2 * i + 1]), sl2, sl2, neg_m, neg_m);
         const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
@@ -948,8 +966,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           s[i] = pack_bf16x2(e0, e1);   // P packed in place: s[i] is already consumed
         }
       }
-      if constexpr (C::TF32) {
+      if constexpr (C::TF32 && C::BN == 128) {
         tmem_st_x128(tS, s);
+      } else if constexpr (C::TF32) {
+        tmem_st_x64(tS, s);
       } else {
         tmem_st_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
       }
@@ -1032,7 +1052,7 @@ cudaError_t launch_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
     if (e != cudaSuccess) return e;
     ready.fetch_or(bit, std::memory_order_acq_rel);
   }
-  const unsigned q_blocks = (p.s_q + kNT * kBM - 1) / (kNT * kBM);
+  const unsigned q_blocks = (p.s_q + C::NT * kBM - 1) / (C::NT * kBM);
   const dim3 grid = CAUSAL ? dim3(p.heads, p.batch, q_blocks) : dim3(q_blocks, p.heads, p.batch);
   // one CTA per SM is resident (its shared memory and registers fill one)
   AttnParams pl = p;
@@ -1065,7 +1085,14 @@ cudaError_t launch_attention(InDtype dt, int head_dim, const CUtensorMap& tm_q,
     return launch_variant<__nv_bfloat16, 64>(tm_q, tm_k, tm_v, p, stream);
   if (dt == InDtype::F32 && head_dim == 64)
     return launch_variant<float, 64>(tm_q, tm_k, tm_v, p, stream);
+  if (dt == InDtype::F32 && head_dim == 128)
+    return launch_variant<float, 128>(tm_q, tm_k, tm_v, p, stream);
   return cudaErrorInvalidValue;
+}
+
+int attn_kv_tile_rows(InDtype dt, int head_dim) {
+  if (dt == InDtype::F32 && head_dim == 128) return Cfg<float, 128>::BN;
+  return dt == InDtype::F32 ? Cfg<float, 64>::BN : Cfg<__nv_bfloat16, 128>::BN;
 }
 
 cudaError_t read_and_clear_device_error(unsigned int* value, cudaStream_t stream) {

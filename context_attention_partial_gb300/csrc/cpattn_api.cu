@@ -87,8 +87,8 @@ int64_t tma_stride(const cpattn_tensor* t, int dim, int64_t dense) {
 }
 
 // 4-D map over a [B, H, S, D] tensor: dims (D, S, H, B), box (128 bytes of D,
-// 128 rows, 1, 1), 128-byte swizzle, zero fill out of bounds.
-cpattn_status make_tmap(CUtensorMap* m, const cpattn_tensor* t) {
+// box_rows rows, 1, 1), 128-byte swizzle, zero fill out of bounds.
+cpattn_status make_tmap(CUtensorMap* m, const cpattn_tensor* t, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return CPATTN_ERR_CUDA;
   const int eb = elem_bytes(t->dtype);
@@ -99,7 +99,7 @@ cpattn_status make_tmap(CUtensorMap* m, const cpattn_tensor* t) {
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)(ss * eb), (cuuint64_t)(sh * eb),
                                  (cuuint64_t)(sb * eb)};
-  const cuuint32_t box[4] = {(cuuint32_t)(128 / eb), 128u, 1u, 1u};
+  const cuuint32_t box[4] = {(cuuint32_t)(128 / eb), (cuuint32_t)box_rows, 1u, 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   const CUtensorMapDataType dt =
       t->dtype == CPATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -176,8 +176,7 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   } else if (!ring_anything && S_kv % ring_degree != 0) {
     return CPATTN_ERR_DIVISIBILITY;
   }
-  const bool supported = (q->dtype == CPATTN_BF16 && (D == 64 || D == 128)) ||
-                         (q->dtype == CPATTN_F32 && D == 64);
+  const bool supported = D == 64 || D == 128;
   if (!supported) return CPATTN_ERR_UNSUPPORTED;
   if (B > 65535 || H > 65535 || S_q > (int64_t(1) << 30) || S_kv > (int64_t(1) << 30))
     return CPATTN_ERR_UNSUPPORTED;
@@ -190,10 +189,12 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
     return CPATTN_ERR_WORKSPACE;
 
+  const InDtype dt = q->dtype == CPATTN_BF16 ? InDtype::BF16 : InDtype::F32;
+  const int kv_rows = cpattn::attn_kv_tile_rows(dt, static_cast<int>(D));
   CUtensorMap tm_q, tm_k, tm_v;
-  if ((st = make_tmap(&tm_q, q)) != CPATTN_OK) return st;
-  if ((st = make_tmap(&tm_k, k)) != CPATTN_OK) return st;
-  if ((st = make_tmap(&tm_v, v)) != CPATTN_OK) return st;
+  if ((st = make_tmap(&tm_q, q, 128)) != CPATTN_OK) return st;
+  if ((st = make_tmap(&tm_k, k, kv_rows)) != CPATTN_OK) return st;
+  if ((st = make_tmap(&tm_v, v, kv_rows)) != CPATTN_OK) return st;
 
   cpattn::AttnParams p;
   std::memset(&p, 0, sizeof(p));
@@ -224,10 +225,10 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
   p.group_heads = group_heads;
   for (int c = 0; c <= ring_degree; ++c) p.chunk_start[c] = chunk_start[c];
   p.n_tiles_all = 0;
-  for (int c = 0; c < ring_degree; ++c) p.n_tiles_all += (chunk_start[c + 1] - chunk_start[c] + 127) / 128;
+  for (int c = 0; c < ring_degree; ++c)
+    p.n_tiles_all += (chunk_start[c + 1] - chunk_start[c] + kv_rows - 1) / kv_rows;
   const cudaError_t e =
-      cpattn::launch_attention(q->dtype == CPATTN_BF16 ? InDtype::BF16 : InDtype::F32,
-                               static_cast<int>(D), tm_q, tm_k, tm_v, p, stream);
+      cpattn::launch_attention(dt, static_cast<int>(D), tm_q, tm_k, tm_v, p, stream);
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 

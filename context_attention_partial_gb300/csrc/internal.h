@@ -41,6 +41,11 @@ struct AttnParams {
 
 enum class InDtype { F32, BF16 };
 
+// Keys per K/V tile of the attention kernel for this input type and head
+// size (the row count of the K and V tensor maps' boxes; query boxes have
+// 128 rows).
+int attn_kv_tile_rows(InDtype dt, int head_dim);
+
 // Launches the attention kernel; tensor maps already encoded.
 cudaError_t launch_attention(InDtype dt, int head_dim, const CUtensorMap& tm_q,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v,

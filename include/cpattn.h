@@ -35,10 +35,11 @@
  *   in the device error word, and the kernel returns.
  * - Scale: scale <= 0 or NaN selects 1/sqrt(D), the scaled_dot_product_attention
  *   default [PARA].
- * - Supported: bf16 inputs with D in {64, 128} (tensor cores, bf16 operands,
- *   fp32 accumulation) and fp32 inputs with D = 64 (tensor cores, tf32
- *   operands, fp32 accumulation).  Anything else: CPATTN_ERR_UNSUPPORTED.
- *   There is no CPU fallback.
+ * - Supported: head size D in {64, 128}, for bf16 inputs (tensor cores, bf16
+ *   operands, fp32 accumulation) and fp32 inputs (tensor cores, tf32
+ *   operands with Q K^T taken as three tf32 products of a high/low split,
+ *   fp32 accumulation).  Anything else: CPATTN_ERR_UNSUPPORTED.  There is
+ *   no CPU fallback.
  */
 #ifndef CPATTN_H_
 #define CPATTN_H_
@@ -127,7 +128,7 @@ size_t cpattn_ring_workspace_bytes(const cpattn_tensor* q, int ring_degree);
  *   ring_anything = 1: any S_kv >= ring_degree; the first S_kv % R chunks are
  *     one key longer ([CP] "Ring Anything Attention"; no mask exists here,
  *     as that variant requires).
- *   q [B, H, S_q, D], k, v [B, H, S_kv, D]: bf16, or f32 with D = 64.
+ *   q [B, H, S_q, D], k, v [B, H, S_kv, D]: bf16 or f32, D = 64 or 128.
  *   out [B, H, S_q, D] same dtype as q (written); lse [B, H, S_q] f32.
  *   workspace: device buffer of at least cpattn_ring_workspace_bytes (16-byte
  *     aligned), may be NULL when ring_degree = 1; its contents on entry do

@@ -9,9 +9,12 @@ Each case is computed once per machine in fp64 and stored as float32 ``.npy``
 files (out and lse) in a cache directory kept out of version control
 (``$CPATTN_ORACLE_CACHE``, default ``_cache/oracle`` at the repository root).
 A case is recomputed when its file is missing or when the oracle source, the
-input generator or the case's own definition changed (a fingerprint is stored
-beside the arrays).  Storing fp32 rounds the fp64 result by at most 2^-24
-relative, far inside the tolerances it is compared at (1e-2, 1e-3).
+case's definition or the generated inputs themselves changed: the stored
+fingerprint covers the bytes of q, k and v, because the seeded generator's
+float32 draws are not bit-identical across CPU architectures and PyTorch
+builds (a cache made on one machine is never trusted on another).  Storing
+fp32 rounds the fp64 result by at most 2^-24 relative, far inside the
+tolerances it is compared at (1e-2, 1e-3).
 
 Expected values (page title, section):
 
@@ -80,13 +83,16 @@ def inputs(case: str):
     return make_qkv(shape, _torch_dtype(dt), seed)
 
 
-def _fingerprint(case: str) -> str:
+def _fingerprint(case: str, qkv=None) -> str:
     h = hashlib.sha256()
     for path in (os.path.join(_HERE, "cpattn_oracle.c"), os.path.join(_HERE, "__init__.py"),
                  os.path.join(ROOT, "workloads.py")):
         with open(path, "rb") as f:
             h.update(f.read())
     h.update(repr(CASES[case]).encode())
+    import torch
+    for t in (qkv if qkv is not None else inputs(case)):
+        h.update(t.contiguous().view(torch.uint8).numpy().tobytes())
     return h.hexdigest()[:16]
 
 
@@ -95,9 +101,9 @@ def _paths(case: str):
     return base + ".out.npy", base + ".lse.npy", base + ".json"
 
 
-def _compute(case: str):
+def _compute(case: str, qkv):
     shape, _, _, how = CASES[case]
-    q, k, v = inputs(case)
+    q, k, v = qkv
     if how[0] == "attention":
         d = shape[-1]
         return oracle.attention(q, k, v, d ** -0.5, causal=how[1])
@@ -110,30 +116,31 @@ def _compute(case: str):
     raise KeyError(case)
 
 
-def fresh(case: str) -> bool:
+def fresh(case: str, qkv=None) -> bool:
     po, pl, pm = _paths(case)
     if not (os.path.exists(po) and os.path.exists(pl) and os.path.exists(pm)):
         return False
     with open(pm) as f:
-        return json.load(f).get("fingerprint") == _fingerprint(case)
+        return json.load(f).get("fingerprint") == _fingerprint(case, qkv)
 
 
 def make(case: str, verbose: bool = False) -> dict:
     """Compute and store one case (unless already fresh); returns its meta."""
     po, pl, pm = _paths(case)
-    if fresh(case):
+    qkv = inputs(case)
+    if fresh(case, qkv):
         with open(pm) as f:
             return json.load(f)
     os.makedirs(CACHE_DIR, exist_ok=True)
     t0 = time.perf_counter()
-    out, lse = _compute(case)
+    out, lse = _compute(case, qkv)
     dt = time.perf_counter() - t0
     tag = f".{os.getpid()}.tmp"
     for arr, path in ((out, po), (lse, pl)):
         with open(path + tag, "wb") as f:
             np.save(f, np.asarray(arr, dtype=np.float32))
         os.replace(path + tag, path)
-    meta = {"case": case, "fingerprint": _fingerprint(case), "oracle_seconds": dt,
+    meta = {"case": case, "fingerprint": _fingerprint(case, qkv), "oracle_seconds": dt,
             "threads": oracle.num_threads(), "out_shape": list(np.shape(out)),
             "lse_shape": list(np.shape(lse))}
     with open(pm + tag, "w") as f:

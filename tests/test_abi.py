@@ -70,8 +70,10 @@ def test_ring_validation():
     assert ring(q, kv, t((1, 2, 256, 128), _lib.F32), R=1) == DTYPE
     assert ring(q, kv, t((1, 2, 255, 128)), R=1) == SHAPE
     assert ring(t((1, 2, 256, 96)), t((1, 2, 256, 96)), t((1, 2, 256, 96))) == UNSUP
+    f = t((1, 2, 256, 96), _lib.F32)
+    assert ring(f, f, f) == UNSUP                                       # D is 64 or 128
     f = t((1, 2, 256, 128), _lib.F32)
-    assert ring(f, f, f) == UNSUP                                       # f32 needs D = 64
+    assert ring(f, f, f, R=2) == WS                                     # f32 D = 128 is served
     # workspace required for R > 1
     assert ring(q, kv, kv, R=2) == WS
     lib_need = lib.cpattn_ring_workspace_bytes(q, 2)

@@ -65,6 +65,8 @@ RING_CASES = [
     (4609, 4609, 64, torch.bfloat16, 2, True, False),
     (77, 256, 64, torch.float32, 4, False, False),
     (300, 301, 64, torch.float32, 3, True, False),
+    (77, 300, 128, torch.float32, 3, False, False),
+    (300, 300, 128, torch.float32, 2, False, True),
     (300, 300, 128, torch.bfloat16, 3, False, True),
     (4609, 4609, 128, torch.bfloat16, 3, True, True),
     (77, 77, 128, torch.bfloat16, 1, False, False),
@@ -101,6 +103,7 @@ def test_ring_writes_only_its_outputs(case):
 @pytest.mark.parametrize("S_q,S_kv,D,dt", [
     (1, 5, 128, torch.bfloat16), (77, 300, 64, torch.bfloat16),
     (4609, 1000, 128, torch.bfloat16), (300, 257, 64, torch.float32),
+    (77, 130, 128, torch.float32),
 ])
 def test_partial_writes_only_its_outputs(S_q, S_kv, D, dt):
     g = torch.Generator("cpu").manual_seed(103)

@@ -178,6 +178,8 @@ PARTIAL_CASES = [
     (1, 2, 256, 128, 128, torch.bfloat16),
     (1, 1, 513, 700, 64, torch.bfloat16),
     (1, 2, 200, 257, 64, torch.float32),
+    (1, 2, 200, 257, 128, torch.float32),         # fp32 D = 128: one query tile, 64-key tiles
+    (2, 3, 1, 1, 128, torch.float32),
 ]
 
 
@@ -208,6 +210,9 @@ RING_CASES = [
     (1, 2, 256, 256, 64, torch.float32, 4, False),       # the tiny workload's layout
     (1, 1, 130, 390, 64, torch.float32, 2, False),
     (1, 2, 64, 1024, 128, torch.bfloat16, 1, False),
+    (1, 2, 256, 256, 128, torch.float32, 4, False),      # fp32 D = 128
+    (1, 1, 130, 391, 128, torch.float32, 3, True),       # 131/130/130, ragged 64-key tiles
+    (1, 24, 1030, 1030, 128, torch.float32, 2, False),   # 216 CTAs: more than one wave
 ]
 
 
@@ -297,6 +302,7 @@ def test_ring_is_deterministic():
     (2, 256, 6, 64, 3, 2, torch.bfloat16),
     (1, 256, 4, 64, 2, 4, torch.float32),
     (1, 130, 4, 128, 4, 1, torch.bfloat16),
+    (1, 256, 4, 128, 2, 2, torch.float32),
 ])
 def test_unified_matches_oracle(b, s, h, d, g, r, dt):
     """Unified (Ulysses x Ring): regroup, ring inside each head group,
@@ -322,6 +328,7 @@ CAUSAL_CASES = [
     (1, 1, 700, 700, 128, torch.bfloat16, 1, False),
     (1, 2, 256, 256, 64, torch.float32, 4, False),
     (1, 1, 77, 13, 128, torch.bfloat16, 13, True),
+    (1, 2, 300, 300, 128, torch.float32, 3, False),
 ]
 
 
@@ -391,6 +398,7 @@ def test_anything_permute_bit_exact(shape, g, dtype):
     (1, 300, 5, 128, 2, torch.bfloat16, False),    # groups 3 2
     (2, 257, 7, 64, 3, torch.bfloat16, False),     # groups 3 2 2
     (1, 256, 5, 64, 3, torch.float32, False),      # fp32 (3xTF32)
+    (1, 200, 5, 128, 3, torch.float32, False),     # fp32, D = 128
     (1, 200, 2, 128, 4, torch.bfloat16, False),    # H < G
     (1, 300, 7, 128, 4, torch.bfloat16, True),     # causal, groups 2 2 2 1
     (1, 130, 8, 128, 4, torch.bfloat16, False),    # even split
@@ -443,7 +451,7 @@ def test_prepared_calls_equal_plain_calls():
     torch.cuda.synchronize()
     status_ok()
     assert torch.equal(call.out, ref[0]) and torch.equal(call.lse, ref[1])
-    x = make_qkv((1, 257, 6, 64), torch.bfloat16, seed=61, device=DEV)
+    x = make_qkv((1, 258, 6, 64), torch.bfloat16, seed=61, device=DEV)
     ref = cp.unified_attention(*x, 2, 2)
     call = cp.prepare_unified(*x, 2, 2)
     call()
