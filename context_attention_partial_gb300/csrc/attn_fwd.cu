@@ -333,12 +333,13 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
     const int row0 = q_row - lane;
     constexpr int64_t es = sizeof(T);
     uint8_t* out_base = static_cast<uint8_t*>(p.out) + (b * p.out_sb + h * p.out_sh) * es;
+    const uint64_t pol_out = l2_policy_evict_first();   // not read again by this kernel
 #pragma unroll
     for (int it = 0; it < kCPR; ++it) {
       const int idx = it * 32 + lane, r = idx / kCPR, c = idx % kCPR;
       if (row0 + r < p.s_q) {
         const uint4 val = reinterpret_cast<const uint4*>(stage)[r * kCPR + (c ^ (r % kCPR))];
-        *reinterpret_cast<uint4*>(out_base + (row0 + r) * p.out_ss * es + c * 16) = val;
+        st_global_v4_hint(out_base + (row0 + r) * p.out_ss * es + c * 16, val, pol_out);
       }
     }
   }
@@ -454,15 +455,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The Q tiles (and, bf16, the first K tile) are requested before the
     // block-wide barrier, so their latency overlaps the rest of the setup.
     mbar_arrive_expect_tx(BAR_Q, C::NT * C::Q_TILE_BYTES);
+    const uint64_t pol_q = l2_policy_evict_first();
     for (int i = 0; i < C::NT; ++i)
       for (int kb = 0; kb < C::NKB; ++kb)
-        tma_load_4d(sQ + i * C::Q_TILE_BYTES + kb * kBM * 128, &tm_q, BAR_Q, kb * C::BOX_COLS,
-                    q_row0 + i * kBM, h, b);
+        tma_load_4d_hint(sQ + i * C::Q_TILE_BYTES + kb * kBM * 128, &tm_q, BAR_Q,
+                         kb * C::BOX_COLS, q_row0 + i * kBM, h, b, pol_q);
     if (!C::TF32 && p.fault_skip_kv == 0) {
       mbar_arrive_expect_tx(bar_full(0), C::KV_TILE_BYTES);
+      const uint64_t pol_kv = l2_policy_evict_last();
       for (int kb = 0; kb < C::NKB; ++kb)
-        tma_load_4d(sKV + kb * C::BN * 128, &tm_k, bar_full(0), kb * C::BOX_COLS, p.chunk_start[0], h,
-                    b);
+        tma_load_4d_hint(sKV + kb * C::BN * 128, &tm_k, bar_full(0), kb * C::BOX_COLS,
+                         p.chunk_start[0], h, b, pol_kv);
     }
   }
   if (warp == kWarpMma) tmem_alloc(smem_addr(tmem_holder), kTmemCols);
@@ -515,10 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // once per tile.  With an even stage count K always lands in an
         // even stage and V in an odd one.
         static_assert(C::STAGES % 2 == 0, "K/V pairing needs an even stage count");
+        const uint64_t pol_kv = l2_policy_evict_last();
         auto load = [&](const CUtensorMap* tm, int stage, uint32_t bar, int key0) {
           for (int kb = 0; kb < C::NKB; ++kb)
-            tma_load_4d(sKV + stage * C::KV_TILE_BYTES + kb * C::BN * 128, tm, bar,
-                        kb * C::BOX_COLS, key0, h, b);
+            tma_load_4d_hint(sKV + stage * C::KV_TILE_BYTES + kb * C::BN * 128, tm, bar,
+                             kb * C::BOX_COLS, key0, h, b, pol_kv);
         };
         if (ok) ld = 1;   // K_0
         for (int j = 0; j < n_tiles && ok; ++j) {
