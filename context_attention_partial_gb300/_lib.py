@@ -15,6 +15,7 @@ STATUS = {
     0: "CPATTN_OK", 1: "CPATTN_ERR_NULL", 2: "CPATTN_ERR_DTYPE", 3: "CPATTN_ERR_SHAPE",
     4: "CPATTN_ERR_DIVISIBILITY", 5: "CPATTN_ERR_LAYOUT", 6: "CPATTN_ERR_UNSUPPORTED",
     7: "CPATTN_ERR_WORKSPACE", 8: "CPATTN_ERR_CUDA", 9: "CPATTN_ERR_TIMEOUT",
+    10: "CPATTN_ERR_BOUNDS",
 }
 F32, BF16 = 0, 1
 
@@ -25,7 +26,7 @@ EXPORTS = (
     "cpattn_set_wait_timeout_ns", "cpattn_ring_noalloc", "cpattn_ring_noalloc_max_workspace_bytes",
     "cpattn_set_fault_injection", "cpattn_ring_causal", "cpattn_ulysses_anything_permute",
     "cpattn_ulysses_anything_attention", "cpattn_ulysses_permute_batch",
-    "cpattn_ulysses_anything_permute_batch",
+    "cpattn_ulysses_anything_permute_batch", "cpattn_is_check_build", "cpattn_set_check_shrink",
 )
 
 
@@ -50,6 +51,47 @@ _lock = threading.Lock()
 _lib = None
 
 
+def bind(path: str):
+    """Opens a build of the library at `path` and declares every function's
+    argument and result types."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(CTensor)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    lib.cpattn_partial.argtypes = [P, P, P, ctypes.c_float, P, P, vp]
+    lib.cpattn_merge.argtypes = [P, P, P, P, vp]
+    lib.cpattn_ring_workspace_bytes.argtypes = [P, i32]
+    lib.cpattn_ring_workspace_bytes.restype = ctypes.c_size_t
+    lib.cpattn_ring.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P, vp, ctypes.c_size_t, vp]
+    lib.cpattn_ulysses_permute.argtypes = [P, i32, i32, P, vp]
+    lib.cpattn_ring_causal.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P, vp,
+                                       ctypes.c_size_t, vp]
+    lib.cpattn_ulysses_anything_permute.argtypes = [P, i32, i32, P, vp]
+    lib.cpattn_ulysses_permute_batch.argtypes = [i32, P, i32, i32, P, vp]
+    lib.cpattn_ulysses_anything_permute_batch.argtypes = [i32, P, i32, i32, P, vp]
+    lib.cpattn_ulysses_anything_attention.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P,
+                                                      vp]
+    lib.cpattn_ring_noalloc.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P, vp]
+    lib.cpattn_ring_noalloc_max_workspace_bytes.argtypes = []
+    lib.cpattn_ring_noalloc_max_workspace_bytes.restype = ctypes.c_size_t
+    lib.cpattn_status_string.argtypes = [i32]
+    lib.cpattn_status_string.restype = ctypes.c_char_p
+    lib.cpattn_last_device_status.argtypes = [vp]
+    lib.cpattn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.cpattn_set_wait_timeout_ns.restype = None
+    lib.cpattn_set_fault_injection.argtypes = [i32]
+    lib.cpattn_set_fault_injection.restype = None
+    lib.cpattn_is_check_build.argtypes = []
+    lib.cpattn_is_check_build.restype = ctypes.c_int
+    lib.cpattn_set_check_shrink.argtypes = [ctypes.c_int64]
+    lib.cpattn_set_check_shrink.restype = None
+    for name in ("cpattn_partial", "cpattn_merge", "cpattn_ring", "cpattn_ulysses_permute",
+                 "cpattn_last_device_status", "cpattn_ring_noalloc", "cpattn_ring_causal",
+                 "cpattn_ulysses_anything_permute", "cpattn_ulysses_anything_attention",
+                 "cpattn_ulysses_permute_batch", "cpattn_ulysses_anything_permute_batch"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
 def load():
     """Loads libcpattn.so (built by ``__graft_entry__.build()``).  Raises if it
     is missing: there is no fallback implementation."""
@@ -61,39 +103,8 @@ def load():
             raise ImportError(
                 f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
                 f"g.build()\"` (nvcc, sm_103a); there is no non-CUDA fallback")
-        lib = ctypes.CDLL(LIB_PATH)
-        P = ctypes.POINTER(CTensor)
-        vp, i32 = ctypes.c_void_p, ctypes.c_int
-        lib.cpattn_partial.argtypes = [P, P, P, ctypes.c_float, P, P, vp]
-        lib.cpattn_merge.argtypes = [P, P, P, P, vp]
-        lib.cpattn_ring_workspace_bytes.argtypes = [P, i32]
-        lib.cpattn_ring_workspace_bytes.restype = ctypes.c_size_t
-        lib.cpattn_ring.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P, vp, ctypes.c_size_t, vp]
-        lib.cpattn_ulysses_permute.argtypes = [P, i32, i32, P, vp]
-        lib.cpattn_ring_causal.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P, vp,
-                                           ctypes.c_size_t, vp]
-        lib.cpattn_ulysses_anything_permute.argtypes = [P, i32, i32, P, vp]
-        lib.cpattn_ulysses_permute_batch.argtypes = [i32, P, i32, i32, P, vp]
-        lib.cpattn_ulysses_anything_permute_batch.argtypes = [i32, P, i32, i32, P, vp]
-        lib.cpattn_ulysses_anything_attention.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P,
-                                                          vp]
-        lib.cpattn_ring_noalloc.argtypes = [P, P, P, ctypes.c_float, i32, i32, P, P, vp]
-        lib.cpattn_ring_noalloc_max_workspace_bytes.argtypes = []
-        lib.cpattn_ring_noalloc_max_workspace_bytes.restype = ctypes.c_size_t
-        lib.cpattn_status_string.argtypes = [i32]
-        lib.cpattn_status_string.restype = ctypes.c_char_p
-        lib.cpattn_last_device_status.argtypes = [vp]
-        lib.cpattn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
-        lib.cpattn_set_wait_timeout_ns.restype = None
-        lib.cpattn_set_fault_injection.argtypes = [i32]
-        lib.cpattn_set_fault_injection.restype = None
-        for name in ("cpattn_partial", "cpattn_merge", "cpattn_ring", "cpattn_ulysses_permute",
-                     "cpattn_last_device_status", "cpattn_ring_noalloc", "cpattn_ring_causal",
-                     "cpattn_ulysses_anything_permute", "cpattn_ulysses_anything_attention",
-                     "cpattn_ulysses_permute_batch", "cpattn_ulysses_anything_permute_batch"):
-            getattr(lib, name).restype = ctypes.c_int
-        _lib = lib
-        return lib
+        _lib = bind(LIB_PATH)
+        return _lib
 
 
 def describe(data_ptr: int, dtype_code: int, shape, stride) -> CTensor:

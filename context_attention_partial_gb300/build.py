@@ -3,6 +3,9 @@
 One object per translation unit, compiled in parallel, linked with the static
 CUDA runtime (the library resolves the driver's tensor-map encoder at run
 time, so it loads on machines without a GPU driver).
+
+``build(check=True)`` builds the bounds-checking variant libcpattn_check.so
+(-DCPATTN_CHECK, a debugging aid with the same ABI) next to it.
 """
 from __future__ import annotations
 
@@ -16,8 +19,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libcpattn.so")
+CHECK_LIB_PATH = os.path.join(PKG, "libcpattn_check.so")
 SOURCES = ["attn_fwd.cu", "merge_permute.cu", "cpattn_api.cu", "ring_noalloc.cu"]
-HEADERS = ["internal.h", "ptx.cuh", "tmem_ops.cuh"]
+HEADERS = ["internal.h", "ptx.cuh", "tmem_ops.cuh", "check.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -28,26 +32,30 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libcpattn.so")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(lib_path: str) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     deps += [os.path.join(ROOT, "include", "cpattn.h"), os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and not _stale():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, check: bool = False) -> str:
+    lib_path = CHECK_LIB_PATH if check else LIB_PATH
+    if not force and not _stale(lib_path):
+        return lib_path
+    build_dir = os.path.join(BUILD_DIR, "check") if check else BUILD_DIR
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                     "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
+    if check:
+        flags.append("-DCPATTN_CHECK")
     flags += list(extra_flags or [])
     procs, objs = [], []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
@@ -63,14 +71,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
             print(text, file=sys.stderr)
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
+    tmp = lib_path + f".{os.getpid()}.tmp"
     link = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(link, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n" + res.stdout + res.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, check="--check" in sys.argv))

@@ -201,6 +201,12 @@ __device__ __forceinline__ float masked_row_max(uint32_t (&s)[N], int valid) {
   return fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
 }
 
+// The running state's LSE of workspace row i (bounds-checked in
+// CPATTN_CHECK builds).
+__device__ __forceinline__ float ws_lse_at(const AttnParams& p, int64_t i) {
+  return CPATTN_IN(p.ws_span, p.ws_lse + i, 4, &g_cpattn_device_error) ? p.ws_lse[i] : 0.f;
+}
+
 // Multiplies this thread's O row (TMEM) by `factor`.
 template <int D>
 __device__ __forceinline__ void rescale_o(uint32_t tO, float factor) {
@@ -289,20 +295,25 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
         } else {
           float4 r[HC / 4];
 #pragma unroll
-          for (int i = 0; i < HC / 4; ++i) r[i] = slot[i * kBM];
+          for (int i = 0; i < HC / 4; ++i)
+            r[i] = CPATTN_IN(p.ws_span, &slot[i * kBM], 16, &g_cpattn_device_error)
+                       ? slot[i * kBM]
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int i = 0; i < HC / 4; ++i) fold(i, r[i]);
         }
       }
       if (!last) {
 #pragma unroll
-        for (int i = 0; i < HC / 4; ++i) slot[i * kBM] = v[i];
+        for (int i = 0; i < HC / 4; ++i)
+          if (CPATTN_IN(p.ws_span, &slot[i * kBM], 16, &g_cpattn_device_error)) slot[i * kBM] = v[i];
       } else if (!staged) {
         // f32 output of bf16 inputs (a single partial): straight to memory
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + b * p.out_sb +
                                                 h * p.out_sh + q_row * p.out_ss + part * HC);
 #pragma unroll
-        for (int i = 0; i < HC / 4; ++i) dst[i] = v[i];
+        for (int i = 0; i < HC / 4; ++i)
+          if (CPATTN_IN(p.out_span, &dst[i], 16, &g_cpattn_device_error)) dst[i] = v[i];
       } else {
         // final output: this lane's row into the warp's staging area
         // (16-byte chunks XOR-swizzled by row against bank conflicts)
@@ -339,15 +350,19 @@ __device__ __forceinline__ void chunk_epilogue(const AttnParams& p, uint32_t tO,
       const int idx = it * 32 + lane, r = idx / kCPR, c = idx % kCPR;
       if (row0 + r < p.s_q) {
         const uint4 val = reinterpret_cast<const uint4*>(stage)[r * kCPR + (c ^ (r % kCPR))];
-        st_global_v4_hint(out_base + (row0 + r) * p.out_ss * es + c * 16, val, pol_out);
+        uint8_t* dst = out_base + (row0 + r) * p.out_ss * es + c * 16;
+        if (CPATTN_IN(p.out_span, dst, 16, &g_cpattn_device_error))
+          st_global_v4_hint(dst, val, pol_out);
       }
     }
   }
   if (row_ok) {
-    if (last)
-      p.lse[b * p.lse_sb + h * p.lse_sh + q_row * p.lse_ss] = lse_new;
-    else
+    if (last) {
+      float* dst = p.lse + (b * p.lse_sb + h * p.lse_sh + q_row * p.lse_ss);
+      if (CPATTN_IN(p.lse_span, dst, 4, &g_cpattn_device_error)) *dst = lse_new;
+    } else if (CPATTN_IN(p.ws_span, ws_lse, 4, &g_cpattn_device_error)) {
       *ws_lse = lse_new;
+    }
   }
   __syncwarp();
 }
@@ -581,11 +596,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             if (leader) {
-              mbar_arrive_expect_tx(bar_ws(i), 2 * C::WS_PIECE_BYTES);
               const char* src = reinterpret_cast<const char*>(p.ws_o) + (tile0 + i) * (kBM * D * 4);
-              for (int k = 2 * i; k < 2 * i + 2; ++k)
-                bulk_load(sQ + ws_piece(k, n_tiles), src + (k % 2) * C::WS_PIECE_BYTES,
-                          C::WS_PIECE_BYTES, bar_ws(i));
+              if (CPATTN_IN(p.ws_span, src, 2 * C::WS_PIECE_BYTES, &g_cpattn_device_error)) {
+                mbar_arrive_expect_tx(bar_ws(i), 2 * C::WS_PIECE_BYTES);
+                for (int k = 2 * i; k < 2 * i + 2; ++k)
+                  bulk_load(sQ + ws_piece(k, n_tiles), src + (k % 2) * C::WS_PIECE_BYTES,
+                            C::WS_PIECE_BYTES, bar_ws(i));
+              } else {
+                mbar_arrive(bar_ws(i));   // (reported; nothing copied)
+              }
             }
             __syncwarp();
             ws_armed = i + 1;
@@ -914,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (w.t == 0 && w.c > 0) {
-        const float lse_run = (w.c > 1 && row_ok) ? p.ws_lse[tile_id * kBM + tile_row] : 0.f;
+        const float lse_run = (w.c > 1 && row_ok) ? ws_lse_at(p, tile_id * kBM + tile_row) : 0.f;
         chunk_epilogue<T, D, false>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok,
                                     tile_id, tile_row, nullptr, lse_run, nullptr, 0u, 0u);
       }
@@ -998,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O is awaited)
       const bool merge = r_eff > 1;
       float lse_run = 0.f;
-      if (kPrefetchState && merge && row_ok) lse_run = p.ws_lse[tile_id * kBM + tile_row];
+      if (kPrefetchState && merge && row_ok) lse_run = ws_lse_at(p, tile_id * kBM + tile_row);
       ok = mbar_wait(bar_o(wg), 0, abort_flag, p.timeout_ns, &g_cpattn_device_error,
                      kErrWaitSoftmax);
       ok = __all_sync(0xffffffffu, ok);
@@ -1010,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
       }
       if (ok) {
-        if (!kPrefetchState && merge && row_ok) lse_run = p.ws_lse[tile_id * kBM + tile_row];
+        if (!kPrefetchState && merge && row_ok) lse_run = ws_lse_at(p, tile_id * kBM + tile_row);
         tc_fence_after();
         // (the state is read only where the epilogue merges, for rows of an
         // existing query tile: exactly where it was prefetched)
@@ -1097,6 +1116,20 @@ cudaError_t launch_attention(InDtype dt, int head_dim, const CUtensorMap& tm_q,
 int attn_kv_tile_rows(InDtype dt, int head_dim) {
   if (dt == InDtype::F32 && head_dim == 128) return Cfg<float, 128>::BN;
   return dt == InDtype::F32 ? Cfg<float, 64>::BN : Cfg<__nv_bfloat16, 128>::BN;
+}
+
+unsigned int* device_error_word() {
+  static std::atomic<unsigned int*> cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  unsigned int* w = cached[dev].load(std::memory_order_acquire);
+  if (w == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_cpattn_device_error) != cudaSuccess) return nullptr;
+    w = static_cast<unsigned int*>(ptr);
+    cached[dev].store(w, std::memory_order_release);
+  }
+  return w;
 }
 
 cudaError_t read_and_clear_device_error(unsigned int* value, cudaStream_t stream) {

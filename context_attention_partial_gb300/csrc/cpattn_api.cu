@@ -24,6 +24,7 @@ using cpattn::InDtype;
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_fault_skip_kv{0};
+std::atomic<long long> g_check_shrink{0};   // testing: output extents shrunk by this many bytes
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -69,6 +70,18 @@ bool shape_ok(const cpattn_tensor* t, int ndim) {
   for (int i = 0; i < ndim; ++i)
     if (t->shape[i] < 0) return false;
   return true;
+}
+
+// Bytes from a tensor's data pointer to the end of its last element (0 if
+// it has none), less `shrink` (the bounds-check testing hook).
+uint64_t extent_bytes(const cpattn_tensor* t, long long shrink = 0) {
+  int64_t last = 0;
+  for (int i = 0; i < t->ndim; ++i) {
+    if (t->shape[i] == 0) return 0;
+    last += (t->shape[i] - 1) * t->stride[i];
+  }
+  const int64_t bytes = (last + 1) * elem_bytes(t->dtype) - shrink;
+  return bytes > 0 ? static_cast<uint64_t>(bytes) : 0;
 }
 
 bool contiguous(const cpattn_tensor* t) {
@@ -210,6 +223,10 @@ cpattn_status run_attention(const cpattn_tensor* q, const cpattn_tensor* k,
     p.ws_o = static_cast<float*>(workspace);
     p.ws_lse = p.ws_o + B * H * ((S_q + 127) / 128) * 128 * D;
   }
+  const long long shrink = g_check_shrink.load();
+  p.out_span = {out->data, extent_bytes(out, shrink)};
+  p.lse_span = {lse->data, extent_bytes(lse, shrink)};
+  p.ws_span = {workspace, need > static_cast<size_t>(shrink) ? need - shrink : 0};
   p.batch = static_cast<int>(B);
   p.heads = static_cast<int>(H);
   p.s_q = static_cast<int>(S_q);
@@ -314,6 +331,10 @@ cpattn_status permute_batch(int n, const cpattn_tensor* x, int degree, int dir, 
   p.degree = degree;
   p.dir = dir;
   p.elem_bytes = elem_bytes(x[0].dtype);
+  const long long shrink = g_check_shrink.load();
+  p.x_bytes = xb;
+  p.y_bytes = yb > static_cast<uintptr_t>(shrink) ? yb - shrink : 0;
+  p.err = cpattn::device_error_word();
   const cudaError_t e =
       anything ? cpattn::launch_permute_anything(p, stream) : cpattn::launch_permute(p, stream);
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
@@ -395,6 +416,12 @@ cpattn_status cpattn_merge(cpattn_tensor* out_a, cpattn_tensor* lse_a, const cpa
     p.lb_s[i] = lse_b->stride[i];
   }
   p.dense = contiguous(out_a) && contiguous(out_b) && contiguous(lse_a) && contiguous(lse_b);
+  const long long shrink = g_check_shrink.load();
+  p.oa_span = {out_a->data, extent_bytes(out_a, shrink)};
+  p.la_span = {lse_a->data, extent_bytes(lse_a, shrink)};
+  p.ob_span = {out_b->data, extent_bytes(out_b)};
+  p.lb_span = {lse_b->data, extent_bytes(lse_b)};
+  p.err = cpattn::device_error_word();
   const cudaError_t e = cpattn::launch_merge(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
@@ -472,6 +499,7 @@ const char* cpattn_status_string(cpattn_status status) {
     case CPATTN_ERR_WORKSPACE: return "workspace missing or too small";
     case CPATTN_ERR_CUDA: return "CUDA runtime error";
     case CPATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    case CPATTN_ERR_BOUNDS: return "device-side bounds check failed (check build)";
   }
   return "unknown status";
 }
@@ -480,11 +508,22 @@ cpattn_status cpattn_last_device_status(void* stream) {
   unsigned int v = 0;
   const cudaError_t e = cpattn::read_and_clear_device_error(&v, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  if (v & cpattn::kErrBounds) return CPATTN_ERR_BOUNDS;
   return v ? CPATTN_ERR_TIMEOUT : CPATTN_OK;
 }
 
 void cpattn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
 
 void cpattn_set_fault_injection(int mode) { g_fault_skip_kv.store(mode == 1 ? 1 : 0); }
+
+void cpattn_set_check_shrink(int64_t bytes) { g_check_shrink.store(bytes > 0 ? bytes : 0); }
+
+int cpattn_is_check_build(void) {
+#ifdef CPATTN_CHECK
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 }  // extern "C"

@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "../../include/cpattn.h"
+#include "check.cuh"
 
 namespace cpattn {
 
@@ -37,6 +38,8 @@ struct AttnParams {
   int n_tiles_all;       // key tiles over all chunks (the count without causal masking)
   int resident_ctas;     // CTAs in flight at once (one per SM; set at launch)
   int chunk_start[CPATTN_MAX_RING_DEGREE + 1];
+  // extents of out, lse and the workspace (checked in CPATTN_CHECK builds)
+  Span out_span, lse_span, ws_span;
 };
 
 enum class InDtype { F32, BF16 };
@@ -61,6 +64,8 @@ struct MergeParams {
   int heads, seq;        // for the strided index map
   int64_t oa_s[3], ob_s[3], la_s[3], lb_s[3];   // strides (b, h, s) in elements
   int dense;             // 1: all four tensors are dense row-major
+  Span oa_span, ob_span, la_span, lb_span;   // (CPATTN_CHECK builds)
+  unsigned int* err;     // device error word
 };
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 
@@ -74,6 +79,8 @@ struct PermuteParams {
   int64_t batch, seq, heads, head_dim, degree;
   int dir;               // +1 forward, -1 inverse
   int elem_bytes;
+  uint64_t x_bytes, y_bytes;   // extent of every x[i] / y[i] (CPATTN_CHECK builds)
+  unsigned int* err;           // device error word
 };
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream);
 // Ulysses Anything regroup between [B, S, H, D] and [G, B, S, ceil(H/G), D]
@@ -82,6 +89,9 @@ cudaError_t launch_permute_anything(const PermuteParams& p, cudaStream_t stream)
 
 // Error word helpers (defined with the device symbol).
 cudaError_t read_and_clear_device_error(unsigned int* value, cudaStream_t stream);
+// Device address of the error word on the current device (nullptr on
+// failure); looked up once per device.
+unsigned int* device_error_word();
 
 // SM count of the current device (152, GB300's, if it cannot be read).
 int sm_count();

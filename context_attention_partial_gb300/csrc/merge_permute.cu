@@ -59,10 +59,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     float a = 0.f, b = 0.f;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
     if (in) {
-      a = p.l_a[la];
-      b = p.l_b[lb];
-      x = *reinterpret_cast<const float4*>(p.o_a + oa);
-      y = __ldcs(reinterpret_cast<const float4*>(p.o_b + ob));
+      if (CPATTN_IN(p.la_span, p.l_a + la, 4, p.err)) a = p.l_a[la];
+      if (CPATTN_IN(p.lb_span, p.l_b + lb, 4, p.err)) b = p.l_b[lb];
+      if (CPATTN_IN(p.oa_span, p.o_a + oa, 16, p.err)) x = *reinterpret_cast<const float4*>(p.o_a + oa);
+      if (CPATTN_IN(p.ob_span, p.o_b + ob, 16, p.err))
+        y = __ldcs(reinterpret_cast<const float4*>(p.o_b + ob));
     }
     __syncwarp();   // every lane of the row has read lse_a before it is overwritten
     if (in) {
@@ -78,8 +79,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
       }
       const float4 o = make_float4(wa * x.x + wb * y.x, wa * x.y + wb * y.y,
                                    wa * x.z + wb * y.z, wa * x.w + wb * y.w);
-      __stcs(reinterpret_cast<float4*>(p.o_a + oa), o);
-      if (cv == 0) p.l_a[la] = lse;
+      if (CPATTN_IN(p.oa_span, p.o_a + oa, 16, p.err)) __stcs(reinterpret_cast<float4*>(p.o_a + oa), o);
+      if (cv == 0 && CPATTN_IN(p.la_span, p.l_a + la, 4, p.err)) p.l_a[la] = lse;
     }
   }
 }
@@ -105,6 +106,8 @@ template <typename V>
 struct PermutePtrs {
   const V* x[kMaxPermuteBatch];
   V* y[kMaxPermuteBatch];
+  uint64_t x_bytes, y_bytes;   // extent of each x / y (CPATTN_CHECK builds)
+  unsigned int* err;           // device error word
 };
 
 // Tensor t's pointers through fixed indices (the parameter block is not
@@ -125,18 +128,20 @@ __global__ void __launch_bounds__(kPermuteThreads)
   V* y;
   permute_pick(ptrs, blockIdx.y, x, y);
   const Index stride = static_cast<Index>(gridDim.x) * blockDim.x;
+  const Span xs{x, ptrs.x_bytes}, ys{y, ptrs.y_bytes};
   for (Index base = static_cast<Index>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
        base += stride * kUnroll) {
     V v[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const Index idx = base + u * stride;
-      if (idx < total) v[u] = __ldcs(x + source_of<Index>(idx, unit, bs, g, dir));
+      const V* src = x + source_of<Index>(idx, unit, bs, g, dir);
+      if (idx < total && CPATTN_IN(xs, src, sizeof(V), ptrs.err)) v[u] = __ldcs(src);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const Index idx = base + u * stride;
-      if (idx < total) __stcs(y + idx, v[u]);
+      if (idx < total && CPATTN_IN(ys, y + idx, sizeof(V), ptrs.err)) __stcs(y + idx, v[u]);
     }
   }
 }
@@ -166,6 +171,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
     g = r + (h - big) / q;
     j = h - big - (g - r) * q;
   }
+  const Span xs{x, ptrs.x_bytes}, ys{y, ptrs.y_bytes};
   const Index flat_base = h * row, flat_step = heads * row;
   const Index grouped_base = (g * bs * hm + j) * row, grouped_step = hm * row;
   const Index stride = static_cast<Index>(gridDim.x) * blockDim.x;
@@ -185,10 +191,12 @@ __global__ void __launch_bounds__(kPermuteThreads)
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
-      if (base + u * stride < per_head) v[u] = __ldcs(x + src[u]);
+      if (base + u * stride < per_head && CPATTN_IN(xs, x + src[u], sizeof(V), ptrs.err))
+        v[u] = __ldcs(x + src[u]);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
-      if (base + u * stride < per_head) __stcs(y + dst[u], v[u]);
+      if (base + u * stride < per_head && CPATTN_IN(ys, y + dst[u], sizeof(V), ptrs.err))
+        __stcs(y + dst[u], v[u]);
   }
 }
 
@@ -199,6 +207,9 @@ PermutePtrs<V> permute_ptrs(const PermuteParams& p) {
     ptrs.x[i] = static_cast<const V*>(p.x[i]);
     ptrs.y[i] = static_cast<V*>(p.y[i]);
   }
+  ptrs.x_bytes = p.x_bytes;
+  ptrs.y_bytes = p.y_bytes;
+  ptrs.err = p.err;
   return ptrs;
 }
 

@@ -61,7 +61,8 @@ typedef enum {
   CPATTN_ERR_UNSUPPORTED = 6,   /* valid, but outside what the kernels cover */
   CPATTN_ERR_WORKSPACE = 7,     /* workspace missing or too small */
   CPATTN_ERR_CUDA = 8,          /* a CUDA runtime call failed */
-  CPATTN_ERR_TIMEOUT = 9        /* a device-side wait ran out of time */
+  CPATTN_ERR_TIMEOUT = 9,       /* a device-side wait ran out of time */
+  CPATTN_ERR_BOUNDS = 10        /* a device-side bounds check failed (check builds only) */
 } cpattn_status;
 
 typedef enum { CPATTN_F32 = 0, CPATTN_BF16 = 1 } cpattn_dtype;
@@ -270,7 +271,8 @@ const char* cpattn_status_string(cpattn_status status);
 /*
  * cpattn_last_device_status -- synchronises `stream`, then reads and clears
  * the device error word that kernel-side waits set when they time out.
- * Returns CPATTN_OK, CPATTN_ERR_TIMEOUT, or CPATTN_ERR_CUDA if the
+ * Returns CPATTN_OK, CPATTN_ERR_TIMEOUT, CPATTN_ERR_BOUNDS (check builds;
+ * reported first when both happened), or CPATTN_ERR_CUDA if the
  * synchronisation itself failed.
  */
 cpattn_status cpattn_last_device_status(void* stream);
@@ -280,6 +282,23 @@ cpattn_status cpattn_last_device_status(void* stream);
  * mbarrier (default 2e9 ns).  Process-wide, read at each launch.
  */
 void cpattn_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Check builds.  The library can also be built with -DCPATTN_CHECK
+ * (libcpattn_check.so; a debugging aid with the same ABI): every global
+ * load and store of the kernels is then tested against the extent of the
+ * buffer it belongs to (the bytes from the descriptor's data pointer to its
+ * last element, or the workspace size); an access outside is skipped and
+ * cpattn_last_device_status reports CPATTN_ERR_BOUNDS.  Nothing traps.
+ * cpattn_is_check_build returns 1 in such a build, 0 otherwise.
+ * cpattn_set_check_shrink (testing hook, process-wide, read at each call):
+ * the extents of every OUTPUT (out, lse, the ring workspace, merge's
+ * out_a/lse_a, a regroup's destination) are taken `bytes` smaller, so a
+ * check build reports the writes to their last bytes and leaves those
+ * bytes untouched; 0 (default) restores them.  No effect in normal builds.
+ */
+int cpattn_is_check_build(void);
+void cpattn_set_check_shrink(int64_t bytes);
 
 /*
  * cpattn_set_fault_injection -- testing hook for the failure path.  mode 1:

@@ -194,3 +194,10 @@ def test_python_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 1, 4, 64)
     with pytest.raises(ValueError):
         cp.partial(q, q, q, out=torch.zeros(1, 1, 4, 64), lse=torch.zeros(1, 1, 4))
+
+
+def test_normal_build_is_not_the_check_build():
+    lib = cp.load_library()
+    assert lib.cpattn_is_check_build() == 0
+    lib.cpattn_set_check_shrink(0)                  # a no-op here
+    assert lib.cpattn_status_string(10) == b"device-side bounds check failed (check build)"
