@@ -80,6 +80,7 @@ def test_ring_validation():
     assert lib_need == 1 * 2 * 256 * (128 + 1) * 4
     assert lib.cpattn_ring_workspace_bytes(q, 1) == 0
     assert ring(q, kv, kv, R=2, ws=FAKE, ws_bytes=lib_need - 4) == WS
+    assert ring(q, kv, kv, R=2, ws=FAKE + 8, ws_bytes=lib_need) == WS   # not 16-byte aligned
     # layout: inner stride must be 1; strides 16-byte multiples; aligned data
     assert ring(t((1, 2, 256, 128), stride=(65536, 32768, 128, 2)), kv, kv) == LAYOUT
     assert ring(t((1, 2, 256, 128), data=FAKE + 2), kv, kv) == LAYOUT

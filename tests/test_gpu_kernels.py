@@ -466,3 +466,25 @@ def test_prepared_calls_equal_plain_calls():
     for g in range(4):
         hg = start[g + 1] - start[g]
         assert torch.equal(call.lse[g, :, :hg], ref[1][g, :, :hg])
+
+
+@pytest.mark.parametrize("skv,anything,causal", [
+    (200, True, False),      # 64 chunks of 3 or 4 keys (Ring Anything)
+    (128, False, False),     # 64 chunks of 2 keys
+    (200, True, True),       # causal: most chunks past a tile's rows are skipped
+])
+def test_ring_at_the_maximum_ring_degree(skv, anything, causal):
+    """ring_degree = CPATTN_MAX_RING_DEGREE (64): the chunk table at its
+    largest, 63 in-kernel merges per query row."""
+    g = torch.Generator("cpu").manual_seed(67)
+    q = torch.randn(1, 2, skv, 128, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 2, skv, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 2, skv, 128, generator=g).to(torch.bfloat16)
+    out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=64, ring_anything=anything,
+                       causal=causal)
+    torch.cuda.synchronize()
+    status_ok()
+    ro, rl = oracle.ring(q, k, v, 128 ** -0.5, ring_degree=64, ring_anything=anything,
+                         causal=causal)
+    assert maxabs(out, ro) <= 1e-2
+    assert maxabs(lse, rl) <= 1e-3
