@@ -828,7 +828,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- fp32 operand prep
       // K_j in place -> K_hi (low 13 mantissa bits cleared), K_lo = K - K_hi
       // into its own tile (same layout); V_j [keys x D] as TMA wrote it ->
-      // Vt [D x keys] (values cleared to tf32 like K_hi), K-major, swizzled.
+      // Vt [D x keys] (values rounded to the nearest tf32: P V is a single
+      // tf32 product, so this rounding and P's are its only error), K-major,
+      // swizzled.
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int lk = 2 * j, sk = lk % C::STAGES;
@@ -867,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = lane; e < C::BN * D; e += 32) {
           const int key = e % C::BN, d = e / C::BN;
           const uint32_t v = *reinterpret_cast<const uint32_t*>(src + sw128_offset(key, d * 4, C::BN));
-          *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = v & 0xFFFFE000u;
+          *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = tf32_rna(u2f(v));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -983,8 +985,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a = 2 * (i & 1);
         fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], e0, e1);
         if constexpr (C::TF32) {
-          s[2 * i] = f2u(e0);
-          s[2 * i + 1] = f2u(e1);
+          // P V reads P as tf32: rounded to nearest here (unbiased; the row
+          // sum keeps the fp32 values, so the LSE stays exact to fp32)
+          s[2 * i] = tf32_rna(e0);
+          s[2 * i + 1] = tf32_rna(e1);
         } else {
           s[i] = pack_bf16x2(e0, e1);   // P packed in place: s[i] is already consumed
         }

@@ -25,6 +25,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// fp32 -> tf32 (10 explicit mantissa bits) rounded to nearest, ties away
+// from zero; the low 13 bits of the result are zero, so a kind::tf32 MMA
+// reads the value exactly.
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t y;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+  return y;
+}
+
 // max of three floats in one instruction (sm_100+).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
