@@ -869,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = lane; e < C::BN * D; e += 32) {
           const int key = e % C::BN, d = e / C::BN;
           const uint32_t v = *reinterpret_cast<const uint32_t*>(src + sw128_offset(key, d * 4, C::BN));
-          *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = tf32_rna(u2f(v));
+          *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = tf32_round_bits(v);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -987,8 +987,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (C::TF32) {
           // P V reads P as tf32: rounded to nearest here (unbiased; the row
           // sum keeps the fp32 values, so the LSE stays exact to fp32)
-          s[2 * i] = tf32_rna(e0);
-          s[2 * i + 1] = tf32_rna(e1);
+          s[2 * i] = tf32_round_bits(f2u(e0));
+          s[2 * i + 1] = tf32_round_bits(f2u(e1));
         } else {
           s[i] = pack_bf16x2(e0, e1);   // P packed in place: s[i] is already consumed
         }

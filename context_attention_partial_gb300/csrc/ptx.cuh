@@ -25,13 +25,16 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// fp32 -> tf32 (10 explicit mantissa bits) rounded to nearest, ties away
-// from zero; the low 13 bits of the result are zero, so a kind::tf32 MMA
-// reads the value exactly.
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-  uint32_t y;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-  return y;
+// fp32 bits -> the nearest tf32 (10 explicit mantissa bits), ties away
+// from zero: half of the dropped range added to the magnitude bits carries
+// into the kept bits exactly when the dropped part is at least half an ulp
+// (into the exponent when the mantissa overflows), then the 13 dropped bits
+// are cleared, so a kind::tf32 MMA reads the value exactly.  Two integer
+// operations: the conversion instruction added three times as much time to
+// the fp32 path.  NaNs whose payload lies only in the dropped bits become
+// infinities, as under truncation.
+__device__ __forceinline__ uint32_t tf32_round_bits(uint32_t x) {
+  return (x + 0x1000u) & 0xFFFFE000u;
 }
 
 // max of three floats in one instruction (sm_100+).
