@@ -12,9 +12,12 @@
 //     lse = max + log1p(exp(min - max)),  o = e^(lse_r - lse) o_r + e^(lse_c - lse) o_c.
 //   With ring_degree = 1 it is a single partial (cpattn_partial).
 //
-// How (one CTA = two 128-row query tiles of one (batch, head); 12 warps):
-//   warp 8      TMA producer: Q once, then K_j, V_j tiles (128 keys) through a
-//               STAGES-deep shared-memory ring (128-byte swizzle).
+// How (one CTA = two 128-row query tiles of one (batch, head) against
+// 128-key K/V tiles; fp32 inputs at D = 128: one query tile against 64-key
+// tiles, see Cfg; 12 warps):
+//   warp 8      TMA producer: Q once, then K_j, V_j tiles through a
+//               STAGES-deep shared-memory ring (128-byte swizzle); query
+//               tiles are marked evict-first in L2, K/V tiles evict-last.
 //   warp 9      MMA issuer (one thread): S_i = Q_i K_j^T into TMEM, then
 //               O_i += P_i V_j with P_i read from TMEM (tcgen05.mma, fp32
 //               accumulation), ping-ponging the two query tiles so the tensor
@@ -23,7 +26,8 @@
 //               (the tf32 MMA kind takes no MN-major B operand).
 //   warps 0-7   softmax, one warpgroup per query tile, one thread per query
 //               row: S row from TMEM -> row max -> 2^(s*scale*log2e - m)
-//               -> row sum, P (bf16, or fp32 for tf32) back into S's columns;
+//               -> row sum, P (bf16, or fp32 rounded to the nearest tf32
+//               for fp32 inputs) back into S's columns;
 //               at each chunk end the normalised partial is merged in fp32
 //               with the running result (held in a global fp32 workspace).
 //   Three quarters through its key tiles, the producer also has the Q
@@ -52,7 +56,8 @@
 
 namespace cpattn {
 
-// Device error word: bit flags of waits that ran out of time; read and
+// Device error word: bit flags of waits that ran out of time (and, in the
+// bounds-checking build, of skipped out-of-extent accesses); read and
 // cleared by the host after a stream synchronisation.
 __device__ unsigned int g_cpattn_device_error = 0;
 
@@ -150,7 +155,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int b, int rows) {
   return (b >> 7) * rows * 128 + r * 128 + ((((b >> 4) & 7) ^ (r & 7)) << 4) + (b & 15);
 }
 
-// Walks the (chunk, tile) sequence shared by all roles.
 // The key tiles of chunk c this CTA visits: all of them, or with causal
 // masking only those starting at or before `kmax`, the CTA's last query row.
 template <int BN>
