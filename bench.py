@@ -7,6 +7,7 @@ LSE merge, epilogue) in one cpattn_ring launch.  Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload flux_ring] [--no-aux] [--no-cpu-baseline]
+  python bench.py --sweep      # one JSON line per shape of a size sweep
 
 Timing: CUDA events on the launching stream around each step; the L2 is
 flushed (a 512 MiB write) between timed steps, outside the events.  Inputs
@@ -608,6 +609,66 @@ def run_reference(args):
     return 0
 
 
+# (batch, heads, seq, head_dim, dtype, ring_degree, ring_anything, causal)
+SWEEP = [
+    (1, 24, 1024, 128, "bf16", 1, False, False),
+    (1, 24, 2048, 128, "bf16", 1, False, False),
+    (1, 24, 4608, 128, "bf16", 1, False, False),
+    (1, 24, 4608, 128, "bf16", 2, False, False),
+    (1, 24, 4608, 128, "bf16", 4, False, False),
+    (1, 24, 8192, 128, "bf16", 2, False, False),
+    (1, 24, 16384, 128, "bf16", 4, False, False),
+    (1, 24, 32768, 128, "bf16", 8, False, False),
+    (4, 24, 4608, 128, "bf16", 2, False, False),
+    (1, 24, 4609, 128, "bf16", 3, True, False),
+    (1, 24, 4608, 128, "bf16", 2, False, True),
+    (1, 24, 16384, 128, "bf16", 4, False, True),
+    (1, 24, 4608, 64, "bf16", 2, False, False),
+    (1, 24, 16384, 64, "bf16", 4, False, False),
+    (1, 8, 4608, 128, "f32", 2, False, False),
+    (1, 8, 4608, 64, "f32", 2, False, False),
+]
+
+
+def run_sweep(args):
+    """Throughput of cpattn_ring over the SWEEP shapes: warm-up steps, then
+    per-step CUDA events with the L2 flushed between steps; one JSON line
+    per shape (inputs drawn on the device from a seeded generator)."""
+    import context_attention_partial_gb300 as cp
+    from workloads import Workload
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    peaks = load_peaks()
+    steps = min(args.steps, 50)
+    for (b, h, sq, d, dt, r, anything, causal) in SWEEP:
+        w = Workload("sweep", b, h, sq, d, dt, ring_degree=r, ring_anything=anything,
+                     causal=causal)
+        g = torch.Generator(device=dev).manual_seed(7)
+        q, k, v = (torch.randn(w.shape, generator=g, device=dev).to(w.torch_dtype)
+                   for _ in range(3))
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
+        need = cp.ring_workspace_bytes(q, r)
+        ws = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+        step = cp.prepare_ring(q, k, v, r, anything, out=out, lse=lse, workspace=ws,
+                               causal=causal)
+        for _ in range(args.warmup):
+            step()
+        times = time_steps(step, steps, flush, stream)
+        if cp.last_device_status() != 0:
+            raise RuntimeError("device status after the sweep step")
+        ms = statistics.median(times)
+        tflops = w.flops / (ms * 1e-3) / 1e12
+        print(json.dumps({"sweep": True, "shape": list(w.shape), "dtype": dt, "ring_degree": r,
+                          "ring_anything": anything, "causal": causal, "ms_median": ms,
+                          "TFLOP/s": tflops, "frac_bf16_peak": tflops / peaks["bf16_tflops"],
+                          "steps": steps}), flush=True)
+        del q, k, v, out, lse, ws, step
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -620,11 +681,15 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="untimed steps before the timed region while clocks are sampled")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time cpattn_ring over a list of shapes, one JSON line each")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 
