@@ -40,7 +40,11 @@
 //   so the last epilogue reads it there instead of from global memory.
 //   setmaxnreg moves registers from the control warpgroup (warps 8-11) to
 //   the two softmax warpgroups.
-//   TMEM (512 columns): S_0 | S_1 | O_0 | O_1.
+//   TMEM (512 columns): S_0 | S_1 | O_0 | O_1, P written over S's first
+//   columns.  bf16 at D = 64: S_0 | S_1 | O_0 | O_1 | P_0 | P_1, so a query
+//   tile's next Q K^T goes out as soon as its softmax has loaded S, without
+//   waiting for its P V (the softmax waits for that P V before it reads or
+//   rescales O or writes P again).
 //   The running max is only raised when it grows by more than 2^8 (exponent
 //   8 in log2 units); between raises P values stay below 256, exact enough
 //   for bf16/fp32 and far from overflow.  The O rescale that a raise needs
@@ -114,7 +118,7 @@ struct Cfg {
   static constexpr int WS_PIECE_BYTES = kBM * (D / 2) * 4;
   static constexpr int WSX_BYTES = TF32 ? 0 : WS_PIECE_BYTES;
   static constexpr int NUM_BARS =
-      1 + 2 * STAGES + 3 * NT + 1 + 2 * VT_BUFS + (TF32 ? 3 : 0) + 2 * NT;
+      1 + 2 * STAGES + 3 * NT + 1 + 2 * VT_BUFS + (TF32 ? 3 : 0) + 4 * NT;
   static constexpr int SMEM_BYTES = 1024 + NT * Q_TILE_BYTES + STAGES * KV_TILE_BYTES +
                                     VT_BUFS * VT_TILE_BYTES + KLO_BYTES + WSX_BYTES +
                                     NUM_BARS * 8 + 16;
@@ -127,9 +131,15 @@ struct Cfg {
   static constexpr uint32_t IDESC_PV = make_idesc(FMT, !TF32, kBM, D);
   static constexpr int O_COL = NT * BN;
   static constexpr int QLO_COL = O_COL + NT * D;   // fp32 inputs: Q_lo of tile i at + i*D
+  // bf16 at D = 64: TMEM has room for P apart from S (S0 S1 O0 O1 P0 P1 =
+  // 128 + 128 + 64 + 64 + 64 + 64 columns), so a query tile's next Q K^T
+  // need not wait for its P V; P of tile i at P_COL + i * BN / 2
+  static constexpr bool SEP_P = !TF32 && D == 64;
+  static constexpr int P_COL = O_COL + NT * D;
   static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte blocks");
   static_assert(O_COL + NT * D <= (int)kTmemCols, "TMEM budget");
   static_assert(!TF32 || QLO_COL + NT * D <= (int)kTmemCols, "tf32 TMEM budget");
+  static_assert(!SEP_P || P_COL + NT * BN / 2 <= (int)kTmemCols, "separate-P TMEM budget");
   static_assert(TF32 || (NT == 2 && BN == 128), "the bf16 MMA schedule ping-pongs two tiles");
   static_assert(!TF32 || STAGES % 2 == 0, "fp32 inputs keep K tiles on even stages");
   static_assert(STAGES >= 2, "need at least two K/V stages");
@@ -410,6 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t BAR_KLO_FULL = BAR_QLO + 8u;
   const uint32_t BAR_KLO_EMPTY = BAR_QLO + 16u;
   auto bar_ws = [&](int i) { return bar0 + 8u * (C::NUM_BARS - 2 * C::NT + i); };
+  // bf16 at D = 64 (separate P): the softmax has S_j of tile i in registers;
+  // P V_j of tile i has completed
+  auto bar_sread = [&](int i) { return bar0 + 8u * (C::NUM_BARS - 4 * C::NT + i); };
+  auto bar_pvdone = [&](int i) { return bar0 + 8u * (C::NUM_BARS - 3 * C::NT + i); };
   // the running state of query tile i is written and fenced for the bulk copy
   auto bar_ws_ready = [&](int i) { return bar0 + 8u * (C::NUM_BARS - C::NT + i); };
   // home of piece k of the final merge's running state (query tile k / 2,
@@ -459,6 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::NT; ++i) {
       mbar_init(bar_ws(i), 1);
       mbar_init(bar_ws_ready(i), 4);   // one arrival per softmax warp
+      mbar_init(bar_sread(i), 4);      // one arrival per softmax warp
+      mbar_init(bar_pvdone(i), 1);
     }
     for (int i = 0; i < C::VT_BUFS; ++i) {
       mbar_init(bar_vt_full(i), 1);
@@ -717,7 +733,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lk = 2 * j + 2, sk = lk % C::STAGES;
         const uint32_t phk = (lk / C::STAGES) & 1;
         const bool more = j + 1 < n_tiles;
-        if constexpr (!C::TF32) {
+        if constexpr (C::SEP_P) {
+          // bf16 at D = 64: P has TMEM of its own, so each query tile's
+          // Q K_{j+1}^T goes out once its softmax has S_j in registers, and
+          // P V_j once P_j is ready (V_j and K_{j+1} arrive together on
+          // K_{j+1}'s barrier; the last V alone on its own)
+          const uint32_t kv_bar = more ? bar_full(sk) : bar_full(sv);
+          const uint32_t kv_ph = more ? phk : 0u;
+          const uint32_t hi = static_cast<uint32_t>(q_desc >> 32);
+          const uint32_t vb = static_cast<uint32_t>(v_desc) + ((sv * C::KV_TILE_BYTES) >> 4);
+          const uint32_t kb = static_cast<uint32_t>(k_desc) + ((sk * C::KV_TILE_BYTES) >> 4);
+          uint32_t vd[C::PV_STEPS], kd[C::QK_STEPS], qd[C::QK_STEPS], pa[C::PV_STEPS];
+#pragma unroll
+          for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+            vd[kk] = vb + ((kk * C::KSTEP * 128) >> 4);
+            pa[kk] = tmem + C::P_COL + kk * C::P_COLS_PER_STEP;
+          }
+#pragma unroll
+          for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+            kd[kk] = kb + (((kk / 4) * (C::BN * 128) + (kk % 4) * 32) >> 4);
+            qd[kk] = static_cast<uint32_t>(q_desc) + (((kk / 4) * (kBM * 128) + (kk % 4) * 32) >> 4);
+          }
+          ok = wait_all(kv_bar, kv_ph, kErrWaitMma);
+          if (!ok) break;
+          if (more) {
+#pragma unroll
+            for (int i = 0; i < C::NT; ++i) {
+              ok = wait_all(bar_sread(i), j & 1, kErrWaitMma);
+              if (!ok) break;
+              tc_fence_after();
+              if (leader) {
+                mma_group<C::QK_STEPS, true>(tmem + i * C::BN, qd, kd, hi, C::IDESC_QK, 0u);
+                mma_commit(bar_s(i));
+                if (i == C::NT - 1) mma_commit(bar_empty(sk));
+              }
+              __syncwarp();
+#pragma unroll
+              for (int kk = 0; kk < C::QK_STEPS; ++kk) qd[kk] += C::Q_TILE_BYTES >> 4;
+            }
+            if (!ok) break;
+          }
+#pragma unroll
+          for (int i = 0; i < C::NT; ++i) {
+            ok = wait_all(bar_p(i), j & 1, kErrWaitMma);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) {
+              mma_group<C::PV_STEPS, false>(tmem + C::O_COL + i * D, pa, vd, hi, C::IDESC_PV, acc);
+              mma_commit(bar_pvdone(i));
+              if (i == C::NT - 1) mma_commit(bar_empty(sv));
+              if (!more) mma_commit(bar_o(i));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int kk = 0; kk < C::PV_STEPS; ++kk) pa[kk] += C::BN / 2;
+          }
+          if (!ok) break;
+        } else if constexpr (!C::TF32) {
           // Every wait that does not depend on the softmax comes first and
           // all descriptors of both groups are built before P_0 is awaited,
           // so that once it is seen only the MMAs are left to issue: this
@@ -938,6 +1010,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      // separate P: P V_{j-1} of this tile must have completed before O is
+      // read or rescaled and before P is overwritten (waited for once)
+      bool pv_done = !C::SEP_P || j == 0;
+      if (C::SEP_P && !pv_done && w.t == 0 && w.c > 0) {
+        ok = mbar_wait(bar_pvdone(wg), (j - 1) & 1, abort_flag, p.timeout_ns,
+                       &g_cpattn_device_error, kErrWaitSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        pv_done = true;
+      }
       if (w.t == 0 && w.c > 0) {
         const float lse_run = (w.c > 1 && row_ok) ? ws_lse_at(p, tile_id * kBM + tile_row) : 0.f;
         chunk_epilogue<T, D, false>(p, tO, w.c - 1, r_eff, m_used, l, b, h, q_row, row_ok,
@@ -960,6 +1043,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_x128(tS, s);
           row_max = masked_row_max<C::BN>(s, valid);
         }
+        if constexpr (C::SEP_P) {
+          // S_j is in registers: Q K_{j+1}^T may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_sread(wg));
+        }
       } else {
         tmem_ld_x64(tS, s);
         row_max = masked_row_max<C::BN>(s, masked ? valid : C::BN);
@@ -976,7 +1065,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= factor;
         need = true;
       }
-      if (__any_sync(0xffffffffu, need)) rescale_o<D>(tO, factor);
+      if (__any_sync(0xffffffffu, need)) {
+        if (C::SEP_P && !pv_done) {
+          ok = mbar_wait(bar_pvdone(wg), (j - 1) & 1, abort_flag, p.timeout_ns,
+                         &g_cpattn_device_error, kErrWaitSoftmax);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          pv_done = true;
+        }
+        rescale_o<D>(tO, factor);
+      }
 
       // a row with every key so far masked keeps m = -inf; its P stays 0
       const float neg_m = (CAUSAL && m_used == -INFINITY) ? 0.f : -m_used;
@@ -1002,7 +1101,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (C::TF32) {
         tmem_st_x64(tS, s);
       } else {
-        tmem_st_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
+        if constexpr (C::SEP_P) {
+          if (!pv_done) {
+            ok = mbar_wait(bar_pvdone(wg), (j - 1) & 1, abort_flag, p.timeout_ns,
+                           &g_cpattn_device_error, kErrWaitSoftmax);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          tmem_st_x64(tmem + lane_base + C::P_COL + wg * (C::BN / 2),
+                      *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
+        } else {
+          tmem_st_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&s[0]));
+        }
       }
       l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
       // the final merge reads the running state through bulk copies: this

@@ -16,7 +16,7 @@ DEV = "cuda:0"
 TIMEOUT = 9
 
 
-@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64),
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 64),
                                      (torch.float32, 128)])
 def test_stalled_producer_times_out_and_recovers(dtype, d):
     lib = cp.load_library()
