@@ -233,20 +233,23 @@ def test_ring_matches_oracle(case):
     assert maxabs(lse, rl) <= tl
 
 
-def test_ring_large_scores_exercise_rescale():
+@pytest.mark.parametrize("d,causal", [(128, False), (64, False), (64, True)])
+def test_ring_large_scores_exercise_rescale(d, causal):
     """Scores with std ~12 make the running max grow by more than 2^8
-    between key tiles, so the in-TMEM output rescale runs.  These inputs are
-    not N(0, 1): the softmax is peaked, outputs reach |v| ~ 4, so the bound is
-    the bf16 half-ulp at [2, 4) (2^-7) plus P's bf16 rounding (2^-9 relative)
-    times max |v| (~4): 2e-2."""
+    between key tiles, so the in-TMEM output rescale runs (at D = 64 after
+    the wait for the tile's previous P V, P having TMEM of its own).  These
+    inputs are not N(0, 1): the softmax is peaked, outputs reach |v| ~ 4, so
+    the bound is the bf16 half-ulp at [2, 4) (2^-7) plus P's bf16 rounding
+    (2^-9 relative) times max |v| (~4): 2e-2."""
     g = torch.Generator("cpu").manual_seed(17)
-    q = (torch.randn(1, 2, 256, 128, generator=g) * 12).to(torch.bfloat16)
-    k = torch.randn(1, 2, 1024, 128, generator=g).to(torch.bfloat16)
-    v = torch.randn(1, 2, 1024, 128, generator=g).to(torch.bfloat16)
-    out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=2)
+    sq = 1024 if causal else 256
+    q = (torch.randn(1, 2, sq, d, generator=g) * 12).to(torch.bfloat16)
+    k = torch.randn(1, 2, 1024, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 2, 1024, d, generator=g).to(torch.bfloat16)
+    out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=2, causal=causal)
     torch.cuda.synchronize()
     status_ok()
-    ro, rl = oracle.ring(q, k, v, 128 ** -0.5, ring_degree=2)
+    ro, rl = oracle.ring(q, k, v, d ** -0.5, ring_degree=2, causal=causal)
     assert maxabs(out, ro) <= 2e-2
     # the LSE bound stays the stated 1e-3 absolute: the scores are exact
     # products of bf16 values summed in fp32 (error ~1e-5 at |lse| ~ 40)
