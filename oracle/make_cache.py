@@ -69,6 +69,9 @@ CASES = {
                          ("ulysses_anything", 5)),
     # bf16 D = 64 over several waves of CTAs (not one of the named workloads)
     "d64_ring": ((2, 24, 4608, 64), "bf16", 61, ("attention", False)),
+    # bf16 D = 64 (P in TMEM columns of its own): causal, and Ring Anything
+    "d64_causal": ((1, 24, 4608, 64), "bf16", 63, ("attention", True)),
+    "d64_uneven": ((2, 24, 4609, 64), "bf16", 65, ("attention", False)),
     # fp32 inputs (3xTF32): D = 128 (one 128-row query tile per CTA, 64-key
     # tiles) over four waves with a ragged tail, and D = 64 causal
     "f32_d128_ring": ((2, 8, 4609, 128), "f32", 71, ("attention", False)),

@@ -162,6 +162,23 @@ def test_ring_d64_many_waves(parity_report):
 
 
 @pytest.mark.parametrize("case, ring_degree, anything, causal",
+                         [("d64_causal", 2, False, True), ("d64_uneven", 3, True, False)])
+def test_ring_d64_causal_and_uneven(parity_report, case, ring_degree, anything, causal):
+    """bf16 D = 64, whose P has TMEM columns of its own (each query tile's
+    next Q K^T goes out before its P V): causal over the FLUX-like length,
+    and Ring Anything over 4609 keys in three uneven chunks."""
+    q, k, v = make_cache.inputs(case)
+    out, lse = cp.ring(q.to(DEV), k.to(DEV), v.to(DEV), ring_degree=ring_degree,
+                       ring_anything=anything, causal=causal)
+    torch.cuda.synchronize()
+    assert cp.last_device_status() == 0
+    if SAMPLED:
+        sampled_bhsd(q, k, v, out, lse, causal, [(0, 0), (0, 23)])
+    else:
+        full_compare(case, out, lse, parity_report)
+
+
+@pytest.mark.parametrize("case, ring_degree, anything, causal",
                          [("f32_d128_ring", 3, True, False), ("f32_d64_causal", 2, False, True)])
 def test_ring_f32(parity_report, case, ring_degree, anything, causal):
     """fp32 inputs through the 3xTF32 path, every element against the
