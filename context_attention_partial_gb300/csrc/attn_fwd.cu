@@ -72,6 +72,7 @@ constexpr int kThreads = 384;     // 3 warpgroups
 constexpr int kWarpProducer = 8;  // warpgroup 2: producer, MMA, V transposer, spare
 constexpr int kWarpMma = 9;
 constexpr int kWarpTranspose = 10;
+constexpr int kTransposeWarps = 2;   // fp32 inputs: warps 10 and 11
 constexpr int kLaunchRegs = 168;  // registers per thread at launch (65536 / 384, rounded down to 8)
 constexpr int kSoftmaxRegs = 208; // after setmaxnreg: 8 x 32 x 208 + 4 x 32 x 88 = 384 x 168
 constexpr int kControlRegs = 88;
@@ -462,7 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_full(s), 1);
       // fp32 inputs: a K stage is released by the MMA and by the K_lo pass
-      mbar_init(bar_empty(s), (C::TF32 && s % 2 == 0) ? 2 : 1);
+      // (fp32 inputs: a K stage is released by the MMA and the transposing
+      // warps, a V stage by the transposing warps)
+      mbar_init(bar_empty(s), C::TF32 ? (s % 2 == 0 ? 1 + kTransposeWarps : kTransposeWarps) : 1);
     }
     for (int i = 0; i < C::NT; ++i) {
       mbar_init(bar_s(i), 1);
@@ -477,12 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_pvdone(i), 1);
     }
     for (int i = 0; i < C::VT_BUFS; ++i) {
-      mbar_init(bar_vt_full(i), 1);
+      mbar_init(bar_vt_full(i), kTransposeWarps);
       mbar_init(bar_vt_empty(i), 1);
     }
     if (C::TF32) {
       mbar_init(BAR_QLO, 4 * C::NT);   // one arrival per softmax warp
-      mbar_init(BAR_KLO_FULL, 1);
+      mbar_init(BAR_KLO_FULL, kTransposeWarps);
       mbar_init(BAR_KLO_EMPTY, 1);
     }
     *abort_flag = 0;
@@ -900,13 +903,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(BAR_DRAIN, 0, p.timeout_ns);
       }
       __syncwarp();
-    } else if (warp == kWarpTranspose && C::TF32) {
+    } else if (warp >= kWarpTranspose && warp < kWarpTranspose + kTransposeWarps && C::TF32) {
       // ---------------------------------------------------------- fp32 operand prep
       // K_j in place -> K_hi (low 13 mantissa bits cleared), K_lo = K - K_hi
       // into its own tile (same layout); V_j [keys x D] as TMA wrote it ->
       // Vt [D x keys] (values rounded to the nearest tf32: P V is a single
       // tf32 product, so this rounding and P's are its only error), K-major,
       // swizzled.
+      // (each of the transposing warps takes every other 32 elements)
+      const int tl = (warp - kWarpTranspose) * 32 + lane;
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int lk = 2 * j, sk = lk % C::STAGES;
@@ -920,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           uint32_t* kt = reinterpret_cast<uint32_t*>(smem + (sKV - sQ) + sk * C::KV_TILE_BYTES);
           uint32_t* klo = reinterpret_cast<uint32_t*>(smem + (sKlo - sQ));
-          for (int e = lane; e < C::KV_TILE_BYTES / 4; e += 32) {
+          for (int e = tl; e < C::KV_TILE_BYTES / 4; e += 32 * kTransposeWarps) {
             const uint32_t x = kt[e], hi = x & 0xFFFFE000u;
             kt[e] = hi;
             klo[e] = f2u(u2f(x) - u2f(hi));
@@ -942,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const uint8_t* src = smem + (sKV - sQ) + sv * C::KV_TILE_BYTES;
         uint8_t* dst = smem + (sVt - sQ) + (j & 1) * C::VT_TILE_BYTES;
-        for (int e = lane; e < C::BN * D; e += 32) {
+        for (int e = tl; e < C::BN * D; e += 32 * kTransposeWarps) {
           const int key = e % C::BN, d = e / C::BN;
           const uint32_t v = *reinterpret_cast<const uint32_t*>(src + sw128_offset(key, d * 4, C::BN));
           *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = tf32_round_bits(v);
