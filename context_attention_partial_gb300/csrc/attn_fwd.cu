@@ -22,8 +22,10 @@
 //               O_i += P_i V_j with P_i read from TMEM (tcgen05.mma, fp32
 //               accumulation), ping-ponging the two query tiles so the tensor
 //               core works on one tile while the other tile's softmax runs.
-//   warp 10     fp32 inputs only: transposes each V tile into a K-major copy
-//               (the tf32 MMA kind takes no MN-major B operand).
+//   warps 10-11 fp32 inputs only: transpose each V tile into a K-major copy
+//               (the tf32 MMA kind takes no MN-major B operand) and split
+//               each K tile into hi/lo parts; with one query tile per CTA
+//               the otherwise idle warps 4-7 share that work.
 //   warps 0-7   softmax, one warpgroup per query tile, one thread per query
 //               row: S row from TMEM -> row max -> 2^(s*scale*log2e - m)
 //               -> row sum, P (bf16, or fp32 rounded to the nearest tf32
@@ -72,7 +74,6 @@ constexpr int kThreads = 384;     // 3 warpgroups
 constexpr int kWarpProducer = 8;  // warpgroup 2: producer, MMA, V transposer, spare
 constexpr int kWarpMma = 9;
 constexpr int kWarpTranspose = 10;
-constexpr int kTransposeWarps = 2;   // fp32 inputs: warps 10 and 11
 constexpr int kLaunchRegs = 168;  // registers per thread at launch (65536 / 384, rounded down to 8)
 constexpr int kSoftmaxRegs = 208; // after setmaxnreg: 8 x 32 x 208 + 4 x 32 x 88 = 384 x 168
 constexpr int kControlRegs = 88;
@@ -105,6 +106,9 @@ struct Cfg {
   // mantissa bits cleared), which keeps scores to about 2^-20 relative; Q_lo
   // sits in TMEM, K_lo in one shared-memory tile.
   static constexpr int VT_BUFS = TF32 ? 2 : 0;
+  // fp32 inputs: warps that transpose V and split K (warps 10 and 11, plus
+  // the second softmax warpgroup when it has no query tile)
+  static constexpr int TP_WARPS = TF32 ? (NT == 1 ? 6 : 2) : 0;
   static constexpr int VT_TILE_BYTES = D * BN * ES;
   static constexpr int KLO_BYTES = TF32 ? KV_TILE_BYTES : 0;
   static constexpr int SMEM_BUDGET = (TF32 ? 226 : 220) * 1024;
@@ -465,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // fp32 inputs: a K stage is released by the MMA and by the K_lo pass
       // (fp32 inputs: a K stage is released by the MMA and the transposing
       // warps, a V stage by the transposing warps)
-      mbar_init(bar_empty(s), C::TF32 ? (s % 2 == 0 ? 1 + kTransposeWarps : kTransposeWarps) : 1);
+      mbar_init(bar_empty(s), C::TF32 ? (s % 2 == 0 ? 1 + C::TP_WARPS : C::TP_WARPS) : 1);
     }
     for (int i = 0; i < C::NT; ++i) {
       mbar_init(bar_s(i), 1);
@@ -480,12 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_pvdone(i), 1);
     }
     for (int i = 0; i < C::VT_BUFS; ++i) {
-      mbar_init(bar_vt_full(i), kTransposeWarps);
+      mbar_init(bar_vt_full(i), C::TP_WARPS);
       mbar_init(bar_vt_empty(i), 1);
     }
     if (C::TF32) {
       mbar_init(BAR_QLO, 4 * C::NT);   // one arrival per softmax warp
-      mbar_init(BAR_KLO_FULL, kTransposeWarps);
+      mbar_init(BAR_KLO_FULL, C::TP_WARPS);
       mbar_init(BAR_KLO_EMPTY, 1);
     }
     *abort_flag = 0;
@@ -528,6 +532,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     n_tiles = 0;
     for (int c = 0; c < r_eff; ++c) n_tiles += chunk_tiles<C::BN>(p, c, kmax);
   }
+
+  // ------------------------------------------------------------ fp32 operand prep
+  // K_j in place -> K_hi (low 13 mantissa bits cleared), K_lo = K - K_hi into
+  // its own tile (same layout); V_j [keys x D] as TMA wrote it -> Vt [D x
+  // keys] (values rounded to the nearest tf32: P V is a single tf32 product,
+  // so this rounding and P's are its only error), K-major, swizzled.  Run by
+  // warps 10 and 11, and with one query tile per CTA also by the idle second
+  // softmax warpgroup: C::TP_WARPS warps in all, warp tw of them taking every
+  // C::TP_WARPS-th group of 32 elements (one warp alone set the fp32 path's
+  // pace).
+  auto transpose_role = [&](int tw) {
+    const int tl = tw * 32 + lane;
+    constexpr int kStride = 32 * (C::TP_WARPS > 0 ? C::TP_WARPS : 1);
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int lk = 2 * j, sk = lk % C::STAGES;
+      ok = mbar_wait(bar_full(sk), (lk / C::STAGES) & 1, abort_flag, p.timeout_ns,
+                     &g_cpattn_device_error, kErrWaitTranspose);
+      if (ok)
+        ok = mbar_wait(BAR_KLO_EMPTY, (j & 1) ^ 1, abort_flag, p.timeout_ns,
+                       &g_cpattn_device_error, kErrWaitTranspose);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      {
+        uint32_t* kt = reinterpret_cast<uint32_t*>(smem + (sKV - sQ) + sk * C::KV_TILE_BYTES);
+        uint32_t* klo = reinterpret_cast<uint32_t*>(smem + (sKlo - sQ));
+        for (int e = tl; e < C::KV_TILE_BYTES / 4; e += kStride) {
+          const uint32_t x = kt[e], hi = x & 0xFFFFE000u;
+          kt[e] = hi;
+          klo[e] = f2u(u2f(x) - u2f(hi));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(BAR_KLO_FULL);
+        mbar_arrive(bar_empty(sk));
+      }
+      const int lv = 2 * j + 1, sv = lv % C::STAGES;
+      ok = mbar_wait(bar_full(sv), (lv / C::STAGES) & 1, abort_flag, p.timeout_ns,
+                     &g_cpattn_device_error, kErrWaitTranspose);
+      if (ok)
+        ok = mbar_wait(bar_vt_empty(j & 1), ((j >> 1) & 1) ^ 1, abort_flag, p.timeout_ns,
+                       &g_cpattn_device_error, kErrWaitTranspose);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const uint8_t* src = smem + (sKV - sQ) + sv * C::KV_TILE_BYTES;
+      uint8_t* dst = smem + (sVt - sQ) + (j & 1) * C::VT_TILE_BYTES;
+      for (int e = tl; e < C::BN * D; e += kStride) {
+        const int key = e % C::BN, d = e / C::BN;
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(src + sw128_offset(key, d * 4, C::BN));
+        *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = tf32_round_bits(v);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_vt_full(j & 1));
+        mbar_arrive(bar_empty(sv));
+      }
+    }
+    __syncwarp();
+  };
 
   if (warp >= 8) {
     regs_decrease<kControlRegs>();
@@ -903,68 +969,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(BAR_DRAIN, 0, p.timeout_ns);
       }
       __syncwarp();
-    } else if (warp >= kWarpTranspose && warp < kWarpTranspose + kTransposeWarps && C::TF32) {
-      // ---------------------------------------------------------- fp32 operand prep
-      // K_j in place -> K_hi (low 13 mantissa bits cleared), K_lo = K - K_hi
-      // into its own tile (same layout); V_j [keys x D] as TMA wrote it ->
-      // Vt [D x keys] (values rounded to the nearest tf32: P V is a single
-      // tf32 product, so this rounding and P's are its only error), K-major,
-      // swizzled.
-      // (each of the transposing warps takes every other 32 elements)
-      const int tl = (warp - kWarpTranspose) * 32 + lane;
-      bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int lk = 2 * j, sk = lk % C::STAGES;
-        ok = mbar_wait(bar_full(sk), (lk / C::STAGES) & 1, abort_flag, p.timeout_ns,
-                       &g_cpattn_device_error, kErrWaitTranspose);
-        if (ok)
-          ok = mbar_wait(BAR_KLO_EMPTY, (j & 1) ^ 1, abort_flag, p.timeout_ns,
-                         &g_cpattn_device_error, kErrWaitTranspose);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        {
-          uint32_t* kt = reinterpret_cast<uint32_t*>(smem + (sKV - sQ) + sk * C::KV_TILE_BYTES);
-          uint32_t* klo = reinterpret_cast<uint32_t*>(smem + (sKlo - sQ));
-          for (int e = tl; e < C::KV_TILE_BYTES / 4; e += 32 * kTransposeWarps) {
-            const uint32_t x = kt[e], hi = x & 0xFFFFE000u;
-            kt[e] = hi;
-            klo[e] = f2u(u2f(x) - u2f(hi));
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(BAR_KLO_FULL);
-          mbar_arrive(bar_empty(sk));
-        }
-        const int lv = 2 * j + 1, sv = lv % C::STAGES;
-        ok = mbar_wait(bar_full(sv), (lv / C::STAGES) & 1, abort_flag, p.timeout_ns,
-                       &g_cpattn_device_error, kErrWaitTranspose);
-        if (ok)
-          ok = mbar_wait(bar_vt_empty(j & 1), ((j >> 1) & 1) ^ 1, abort_flag, p.timeout_ns,
-                         &g_cpattn_device_error, kErrWaitTranspose);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        const uint8_t* src = smem + (sKV - sQ) + sv * C::KV_TILE_BYTES;
-        uint8_t* dst = smem + (sVt - sQ) + (j & 1) * C::VT_TILE_BYTES;
-        for (int e = tl; e < C::BN * D; e += 32 * kTransposeWarps) {
-          const int key = e % C::BN, d = e / C::BN;
-          const uint32_t v = *reinterpret_cast<const uint32_t*>(src + sw128_offset(key, d * 4, C::BN));
-          *reinterpret_cast<uint32_t*>(dst + sw128_offset(d, key * 4, D)) = tf32_round_bits(v);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar_vt_full(j & 1));
-          mbar_arrive(bar_empty(sv));
-        }
-      }
-      __syncwarp();
+    } else if (warp >= kWarpTranspose && warp < kWarpTranspose + 2 && C::TF32) {
+      transpose_role(warp - kWarpTranspose);
     }
+  } else if (C::TF32 && C::NT == 1 && warp >= 4 && warp < 8) {
+    transpose_role(2 + warp - 4);
   } else if (warp / 4 < C::NT) {
     // ------------------------------------------------------------ softmax
-    // (one warpgroup per query tile; with a single query tile per CTA the
-    // second softmax warpgroup has no work and waits at the final barrier)
+    // (one warpgroup per query tile; with a single query tile per CTA, fp32
+    // inputs at D = 128, the second warpgroup transposes V instead)
     regs_increase<kSoftmaxRegs>();
     const int wg = warp / 4;
     const int quarter = warp % 4;
